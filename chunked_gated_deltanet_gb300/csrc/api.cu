@@ -1,0 +1,366 @@
+// C ABI of the library (declared in include/gdn.h): argument validation on the
+// host before any device work, workspace layout, and launch orchestration.
+#include "gdn.h"
+#include "common.cuh"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#define GDN_API extern "C" __attribute__((visibility("default")))
+
+using gdn::kBlock;
+using gdn::LaunchCommon;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+gdn_status fail(gdn_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+gdn_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t channels(const gdn_layer_desc *d) {
+    return 2LL * d->n_qk_heads * d->d_k + (int64_t)d->n_v_heads * d->d_v;
+}
+
+size_t in_elt(const gdn_layer_desc *d) { return d->in_dtype == GDN_BF16 ? 2 : 4; }
+
+gdn_status check_desc(const gdn_layer_desc *d) {
+    if (!d) return fail(GDN_ERR_INVALID_ARG, "layer description is NULL");
+    if (d->n_qk_heads < 1 || d->n_v_heads < 1 || d->n_v_heads % d->n_qk_heads != 0 || d->n_v_heads > 65535)
+        return fail(GDN_ERR_SHAPE, "heads: need 1 <= Hk, Hv a multiple of Hk, Hv <= 65535 (Hk=%d, Hv=%d)",
+                    d->n_qk_heads, d->n_v_heads);
+    if ((d->d_k != 64 && d->d_k != 128) || d->d_v != d->d_k)
+        return fail(GDN_ERR_SHAPE, "head dims: need d_k = d_v in {64, 128} (d_k=%d, d_v=%d)", d->d_k, d->d_v);
+    if (d->grid_c < 64 || d->grid_c > 4096 || d->grid_c % 64 != 0)
+        return fail(GDN_ERR_SHAPE, "grid_c must be a multiple of 64 in [64, 4096] (got %d)", d->grid_c);
+    if (d->in_dtype != GDN_BF16 && d->in_dtype != GDN_FP32)
+        return fail(GDN_ERR_SHAPE, "in_dtype must be GDN_BF16 or GDN_FP32 (got %d)", d->in_dtype);
+    if (d->out_dtype != GDN_BF16 && d->out_dtype != GDN_FP32)
+        return fail(GDN_ERR_SHAPE, "out_dtype must be GDN_BF16 or GDN_FP32 (got %d)", d->out_dtype);
+    if (d->conv_act != GDN_CONV_NONE && d->conv_act != GDN_CONV_SILU)
+        return fail(GDN_ERR_SHAPE, "conv_act must be GDN_CONV_NONE or GDN_CONV_SILU (got %d)", d->conv_act);
+    if (!(d->l2_eps > 0.f) || !std::isfinite(d->l2_eps) || !std::isfinite(d->q_scale))
+        return fail(GDN_ERR_INVALID_ARG, "l2_eps must be finite and > 0, q_scale finite");
+    return GDN_OK;
+}
+
+uint64_t tag_of(const gdn_layer_desc *d) {
+    // FNV-1a over a format version and every field of the description
+    uint64_t h = 1469598103934665603ULL;
+    auto mix = [&](uint32_t v) {
+        for (int i = 0; i < 4; ++i) { h ^= (v >> (8 * i)) & 0xffu; h *= 1099511628211ULL; }
+    };
+    mix(0x31444447u);  // "GDD1": state layout version
+    const int32_t f[8] = {d->n_qk_heads, d->n_v_heads, d->d_k, d->d_v, d->grid_c, d->in_dtype, d->out_dtype, d->conv_act};
+    for (int32_t v : f) mix((uint32_t)v);
+    uint32_t b;
+    std::memcpy(&b, &d->q_scale, 4); mix(b);
+    std::memcpy(&b, &d->l2_eps, 4); mix(b);
+    return h ? h : 1;
+}
+
+gdn_status check_state(const gdn_layer_desc *d, const gdn_session *s, const char *what, bool need_present) {
+    if (!s) return fail(GDN_ERR_INVALID_ARG, "%s is NULL", what);
+    if (!s->S || !s->conv || !aligned16(s->S) || !aligned16(s->conv))
+        return fail(GDN_ERR_INVALID_ARG, "%s: S and conv must be non-NULL and 16-byte aligned", what);
+    if (s->tag != tag_of(d))
+        return fail(GDN_ERR_STATE_MISMATCH, "%s belongs to another layer description (tag %llx, expected %llx)",
+                    what, (unsigned long long)s->tag, (unsigned long long)tag_of(d));
+    if (need_present && s->committed < 0)
+        return fail(GDN_ERR_STATE_MISMATCH, "%s is a missing slot (committed = %lld)", what, (long long)s->committed);
+    return GDN_OK;
+}
+
+// Workspace layout for a launch of up to nblk blocks.
+struct WsLayout {
+    size_t qk_off, wu_off, bytes;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const gdn_layer_desc *d, int64_t nblk) {
+    WsLayout L;
+    const int D = d->d_k;
+    L.qk_off = 0;
+    L.wu_off = align256((size_t)nblk * d->n_qk_heads * gdn::qk_floats(D) * sizeof(float));
+    L.bytes = L.wu_off + align256((size_t)nblk * d->n_v_heads * gdn::wu_floats(D) * sizeof(float));
+    return L;
+}
+
+void fill_common(LaunchCommon &p, const gdn_layer_desc *d, const void *xq, const void *xk, const void *xv,
+                 const float *g, const float *beta, const void *conv_w, void *out) {
+    std::memset(&p, 0, sizeof(p));
+    p.xq = xq; p.xk = xk; p.xv = xv; p.g = g; p.beta = beta; p.conv_w = conv_w; p.out = out;
+    p.Hk = d->n_qk_heads; p.Hv = d->n_v_heads; p.G = d->n_v_heads / d->n_qk_heads;
+    p.act = d->conv_act; p.out_bf16 = d->out_dtype == GDN_BF16;
+    p.q_scale = d->q_scale; p.eps = d->l2_eps;
+}
+
+}  // namespace
+
+GDN_API uint64_t gdn_desc_tag(const gdn_layer_desc *desc) {
+    if (check_desc(desc) != GDN_OK) return 0;
+    return tag_of(desc);
+}
+
+GDN_API gdn_status gdn_desc_check(const gdn_layer_desc *desc) { return check_desc(desc); }
+
+GDN_API size_t gdn_state_bytes(const gdn_layer_desc *d) {
+    if (check_desc(d) != GDN_OK) return 0;
+    return (size_t)d->n_v_heads * d->d_k * d->d_v * sizeof(float);
+}
+
+GDN_API size_t gdn_conv_state_bytes(const gdn_layer_desc *d) {
+    if (check_desc(d) != GDN_OK) return 0;
+    return 3 * (size_t)channels(d) * in_elt(d);
+}
+
+GDN_API gdn_status gdn_session_init(const gdn_layer_desc *d, gdn_session *s, float *S, void *conv,
+                                    gdn_stream_t stream) {
+    gdn_status st = check_desc(d);
+    if (st != GDN_OK) return st;
+    if (!s) return fail(GDN_ERR_INVALID_ARG, "session is NULL");
+    if (!S || !conv || !aligned16(S) || !aligned16(conv))
+        return fail(GDN_ERR_INVALID_ARG, "S and conv must be non-NULL and 16-byte aligned");
+    cudaError_t e = gdn_launch_copy(S, nullptr, gdn_state_bytes(d), conv, nullptr, gdn_conv_state_bytes(d),
+                                    (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "session zeroing");
+    s->S = S; s->conv = conv; s->committed = 0; s->tag = tag_of(d);
+    return GDN_OK;
+}
+
+GDN_API size_t gdn_workspace_size(const gdn_layer_desc *d, int64_t max_tokens, int32_t max_sessions) {
+    if (check_desc(d) != GDN_OK || max_tokens < 0 || max_sessions < 1) return 0;
+    const int64_t per_launch = std::min<int64_t>(max_sessions, gdn::kLaunchSessions);
+    const int64_t nblk = (max_tokens + kBlock - 1) / kBlock + per_launch;
+    return ws_layout(d, nblk).bytes;
+}
+
+GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sessions, int32_t n_sessions,
+                                      const int64_t *cu, const void *xq, const void *xk, const void *xv,
+                                      const float *g, const float *beta, const void *conv_w, uint32_t flags,
+                                      void *out, int64_t *n_consumed, void *workspace, size_t workspace_bytes,
+                                      gdn_stream_t stream) {
+    gdn_status st = check_desc(d);
+    if (st != GDN_OK) return st;
+    if (flags & ~GDN_ALLOW_PARTIAL) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
+    if (n_sessions < 1 || n_sessions > GDN_MAX_SESSIONS)
+        return fail(GDN_ERR_INVALID_ARG, "n_sessions must be in [1, %d] (got %d)", GDN_MAX_SESSIONS, n_sessions);
+    if (!sessions || !cu || !n_consumed) return fail(GDN_ERR_INVALID_ARG, "sessions, cu_seqlens, n_consumed must be non-NULL");
+    if (cu[0] != 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens[0] must be 0 (got %lld)", (long long)cu[0]);
+    const bool partial = flags & GDN_ALLOW_PARTIAL;
+    const int C = d->grid_c;
+    std::vector<int64_t> nproc(n_sessions);
+    int64_t total = 0;
+    for (int i = 0; i < n_sessions; ++i) {
+        const int64_t len = cu[i + 1] - cu[i];
+        if (len < 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens must be non-decreasing (at %d)", i);
+        if (len > (int64_t)1 << 30) return fail(GDN_ERR_INVALID_ARG, "session %d: more than 2^30 tokens in one call", i);
+        char what[48];
+        snprintf(what, sizeof(what), "session %d", i);
+        if ((st = check_state(d, &sessions[i], what, true)) != GDN_OK) return st;
+        if (!partial && sessions[i].committed % C != 0)
+            return fail(GDN_ERR_OFF_GRID, "session %d is off grid (committed %lld, grid %d): only a partial call, "
+                        "a decode step or a restore may follow", i, (long long)sessions[i].committed, C);
+        nproc[i] = partial ? len : (len / C) * C;
+        total += nproc[i];
+    }
+    {
+        std::vector<const void *> ptrs(n_sessions);
+        for (int i = 0; i < n_sessions; ++i) ptrs[i] = sessions[i].S;
+        std::sort(ptrs.begin(), ptrs.end());
+        if (std::adjacent_find(ptrs.begin(), ptrs.end()) != ptrs.end())
+            return fail(GDN_ERR_INVALID_ARG, "the sessions of one call must be distinct");
+    }
+    // blocks per launch batch, and the workspace that needs
+    int64_t max_batch_blocks = 0;
+    for (int i0 = 0; i0 < n_sessions;) {
+        int64_t nb = 0;
+        int cnt = 0, i = i0;
+        for (; i < n_sessions && cnt < gdn::kLaunchSessions; ++i)
+            if (nproc[i] > 0) { nb += (nproc[i] + kBlock - 1) / kBlock; ++cnt; }
+        max_batch_blocks = std::max(max_batch_blocks, nb);
+        i0 = i;
+    }
+    if (total > 0) {
+        if (!xq || !xk || !xv || !g || !beta || !conv_w || !out)
+            return fail(GDN_ERR_INVALID_ARG, "input / output pointers must be non-NULL");
+        if (!aligned16(xq) || !aligned16(xk) || !aligned16(xv) || !aligned16(conv_w) || !aligned16(out) ||
+            (reinterpret_cast<uintptr_t>(g) & 3) || (reinterpret_cast<uintptr_t>(beta) & 3))
+            return fail(GDN_ERR_INVALID_ARG, "xq, xk, xv, conv_w, out must be 16-byte aligned; g, beta 4-byte aligned");
+        const WsLayout L = ws_layout(d, max_batch_blocks);
+        if (!workspace || !aligned16(workspace) || workspace_bytes < L.bytes)
+            return fail(GDN_ERR_WORKSPACE, "workspace needs %zu bytes (16-byte aligned), got %zu", L.bytes,
+                        workspace ? workspace_bytes : (size_t)0);
+        if (max_batch_blocks > INT32_MAX) return fail(GDN_ERR_INVALID_ARG, "too many blocks in one call");
+    }
+
+    // launches, in batches of up to kLaunchSessions sessions
+    const int D = d->d_k;
+    const int64_t ch = channels(d);
+    const int in_bf16 = d->in_dtype == GDN_BF16;
+    cudaStream_t cst = (cudaStream_t)stream;
+    if (total > 0) {
+        const WsLayout L = ws_layout(d, max_batch_blocks);
+        static_assert(sizeof(LaunchCommon) <= 4096, "launch parameters must fit the 4 KB limit");
+        LaunchCommon p;
+        fill_common(p, d, xq, xk, xv, g, beta, conv_w, out);
+        p.ws_qk = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.qk_off);
+        p.ws_wu = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.wu_off);
+        for (int i0 = 0; i0 < n_sessions;) {
+            int cnt = 0, i = i0, blk = 0;
+            for (; i < n_sessions && cnt < gdn::kLaunchSessions; ++i) {
+                if (nproc[i] <= 0) continue;
+                gdn::SessRef &r = p.s[cnt++];
+                r.row0 = cu[i]; r.n = (int32_t)nproc[i]; r.blk0 = blk;
+                r.S = sessions[i].S; r.conv = sessions[i].conv;
+                blk += (int)((nproc[i] + kBlock - 1) / kBlock);
+            }
+            i0 = i;
+            if (cnt == 0) continue;
+            p.n_sess = cnt; p.nblk = blk;
+            cudaError_t e = gdn_launch_prep(p, D, in_bf16, ch, cst);
+            if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
+            e = gdn_launch_conv_commit(p, D, in_bf16, ch, cst);
+            if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
+            e = gdn_launch_state(p, D, cst);
+            if (e != cudaSuccess) return cuda_fail(e, "state/output kernel");
+        }
+    }
+    for (int i = 0; i < n_sessions; ++i) {
+        sessions[i].committed += nproc[i];
+        n_consumed[i] = nproc[i];
+    }
+    return GDN_OK;
+}
+
+GDN_API gdn_status gdn_prefill_chunks(const gdn_layer_desc *d, gdn_session *session, const void *xq,
+                                      const void *xk, const void *xv, const float *g, const float *beta,
+                                      const void *conv_w, int64_t n_tokens, uint32_t flags, void *out,
+                                      int64_t *n_consumed, void *workspace, size_t workspace_bytes,
+                                      gdn_stream_t stream) {
+    if (n_tokens < 0) return fail(GDN_ERR_INVALID_ARG, "n_tokens must be >= 0 (got %lld)", (long long)n_tokens);
+    const int64_t cu[2] = {0, n_tokens};
+    return gdn_prefill_varlen(d, session, 1, cu, xq, xk, xv, g, beta, conv_w, flags, out, n_consumed, workspace,
+                              workspace_bytes, stream);
+}
+
+GDN_API gdn_status gdn_state_capture(const gdn_layer_desc *d, const gdn_session *src, gdn_session *slot,
+                                     gdn_stream_t stream) {
+    gdn_status st = check_desc(d);
+    if (st != GDN_OK) return st;
+    if ((st = check_state(d, src, "source session", true)) != GDN_OK) return st;
+    if (!slot || !slot->S || !slot->conv || !aligned16(slot->S) || !aligned16(slot->conv))
+        return fail(GDN_ERR_INVALID_ARG, "slot buffers must be non-NULL and 16-byte aligned");
+    if (slot->S == src->S) return fail(GDN_ERR_INVALID_ARG, "slot and source share their buffers");
+    slot->committed = -1;  // missing until the copy is enqueued
+    slot->tag = 0;
+    cudaError_t e = gdn_launch_copy(slot->S, src->S, gdn_state_bytes(d), slot->conv, src->conv,
+                                    gdn_conv_state_bytes(d), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "state capture copy");
+    slot->committed = src->committed;
+    slot->tag = src->tag;
+    return GDN_OK;
+}
+
+GDN_API gdn_status gdn_state_restore(const gdn_layer_desc *d, gdn_session *dst, const gdn_session *slot,
+                                     gdn_stream_t stream) {
+    gdn_status st = check_desc(d);
+    if (st != GDN_OK) return st;
+    if ((st = check_state(d, slot, "slot", true)) != GDN_OK) return st;
+    if ((st = check_state(d, dst, "destination session", false)) != GDN_OK) return st;
+    if (slot->S == dst->S) return fail(GDN_ERR_INVALID_ARG, "slot and destination share their buffers");
+    cudaError_t e = gdn_launch_copy(dst->S, slot->S, gdn_state_bytes(d), dst->conv, slot->conv,
+                                    gdn_conv_state_bytes(d), (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "state restore copy");
+    dst->committed = slot->committed;
+    return GDN_OK;
+}
+
+GDN_API gdn_status gdn_conv_state(const gdn_layer_desc *d, const gdn_session *s, void *out, gdn_stream_t stream) {
+    gdn_status st = check_desc(d);
+    if (st != GDN_OK) return st;
+    if ((st = check_state(d, s, "session", true)) != GDN_OK) return st;
+    if (!out) return fail(GDN_ERR_INVALID_ARG, "out is NULL");
+    cudaError_t e = cudaMemcpyAsync(out, s->conv, gdn_conv_state_bytes(d), cudaMemcpyDefault, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "conv state copy");
+    return GDN_OK;
+}
+
+GDN_API gdn_status gdn_decode_step(const gdn_layer_desc *d, gdn_session *sessions, int32_t n, const void *xq,
+                                   const void *xk, const void *xv, const float *g, const float *beta,
+                                   const void *conv_w, void *out, gdn_stream_t stream) {
+    gdn_status st = check_desc(d);
+    if (st != GDN_OK) return st;
+    if (n < 1 || n > GDN_MAX_SESSIONS)
+        return fail(GDN_ERR_INVALID_ARG, "n_sessions must be in [1, %d] (got %d)", GDN_MAX_SESSIONS, n);
+    if (!sessions) return fail(GDN_ERR_INVALID_ARG, "sessions is NULL");
+    for (int i = 0; i < n; ++i) {
+        char what[48];
+        snprintf(what, sizeof(what), "session %d", i);
+        if ((st = check_state(d, &sessions[i], what, true)) != GDN_OK) return st;
+    }
+    {
+        std::vector<const void *> ptrs(n);
+        for (int i = 0; i < n; ++i) ptrs[i] = sessions[i].S;
+        std::sort(ptrs.begin(), ptrs.end());
+        if (std::adjacent_find(ptrs.begin(), ptrs.end()) != ptrs.end())
+            return fail(GDN_ERR_INVALID_ARG, "the sessions of one call must be distinct");
+    }
+    if (!xq || !xk || !xv || !g || !beta || !conv_w || !out)
+        return fail(GDN_ERR_INVALID_ARG, "input / output pointers must be non-NULL");
+    if (!aligned16(xq) || !aligned16(xk) || !aligned16(xv) || !aligned16(conv_w) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(g) & 3) || (reinterpret_cast<uintptr_t>(beta) & 3))
+        return fail(GDN_ERR_INVALID_ARG, "xq, xk, xv, conv_w, out must be 16-byte aligned; g, beta 4-byte aligned");
+    const int D = d->d_k;
+    const int64_t ch = channels(d);
+    const int in_bf16 = d->in_dtype == GDN_BF16;
+    LaunchCommon p;
+    fill_common(p, d, xq, xk, xv, g, beta, conv_w, out);
+    for (int i0 = 0; i0 < n; i0 += gdn::kLaunchSessions) {
+        const int cnt = std::min(n - i0, gdn::kLaunchSessions);
+        for (int j = 0; j < cnt; ++j) {
+            gdn::SessRef &r = p.s[j];
+            r.row0 = i0 + j; r.n = 1; r.blk0 = 0;
+            r.S = sessions[i0 + j].S; r.conv = sessions[i0 + j].conv;
+        }
+        p.n_sess = cnt; p.nblk = 0;
+        cudaError_t e = gdn_launch_decode(p, D, in_bf16, ch, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+        e = gdn_launch_conv_commit(p, D, in_bf16, ch, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
+    }
+    for (int i = 0; i < n; ++i) sessions[i].committed += 1;
+    return GDN_OK;
+}
+
+GDN_API const char *gdn_last_error(void) { return g_err; }
+
+GDN_API const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+        case GDN_ERR_SHAPE: return "GDN_ERR_SHAPE";
+        case GDN_ERR_OFF_GRID: return "GDN_ERR_OFF_GRID";
+        case GDN_ERR_STATE_MISMATCH: return "GDN_ERR_STATE_MISMATCH";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    }
+    return "unknown status";
+}

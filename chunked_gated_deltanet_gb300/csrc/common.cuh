@@ -1,0 +1,72 @@
+// Internal definitions shared by the library's kernels and its C ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kBlock = 64;           // tokens per compute block (divides every grid C)
+constexpr int kLaunchSessions = 64;  // sessions described by one launch's parameters
+constexpr int kThreads = 256;
+
+// One session's slice of a launch.
+struct SessRef {
+    int64_t row0;    // first row of the session's tokens in the packed inputs / outputs
+    int32_t n;       // tokens processed for this session in this call
+    int32_t blk0;    // index of its first 64-token block in the launch's block numbering
+    float *S;        // fp32 [Hv][D][D] state (transposed)
+    void *conv;      // in_dtype [3][ch] conv state
+};
+
+struct LaunchCommon {
+    const void *xq, *xk, *xv;   // packed inputs
+    const float *g, *beta;      // [rows][Hv]
+    const void *conv_w;         // [ch][4]
+    void *out;                  // [rows][Hv][D]
+    float *ws_qk;               // [nblk][Hk][2][64][D]   q_hat, k_hat
+    float *ws_wu;               // [nblk][Hv][wu_floats]  W, U, P, gamma
+    int Hk, Hv, G;
+    int act, out_bf16;
+    float q_scale, eps;
+    int n_sess;
+    int nblk;                   // total blocks of this launch
+    SessRef s[kLaunchSessions];
+};
+
+// Per-(block, v-head) record in the workspace: W [64][D], U [64][D], P [64][64], gamma [64].
+__host__ __device__ constexpr int64_t wu_floats(int D) { return 2LL * kBlock * D + kBlock * kBlock + kBlock; }
+__host__ __device__ constexpr int64_t qk_floats(int D) { return 2LL * kBlock * D; }
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ int find_session(const LaunchCommon &p, int blk) {
+    int s = 0;
+    while (s + 1 < p.n_sess && p.s[s + 1].blk0 <= blk) ++s;
+    return s;
+}
+
+// Causal conv of one channel over a 64-row block, fixed fma order (oldest tap first).
+// x_at(i) returns the raw input at block row i (i in [-3, n)), zero is used past n.
+template <typename InT>
+__device__ __forceinline__ float conv_tap(const float w[4], float xm3, float xm2, float xm1, float x0, int act) {
+    float acc = w[0] * xm3;
+    acc = fmaf(w[1], xm2, acc);
+    acc = fmaf(w[2], xm1, acc);
+    acc = fmaf(w[3], x0, acc);
+    if (act) acc = acc / (1.0f + expf(-acc));
+    return acc;
+}
+
+}  // namespace gdn
+
+// Launchers (host). Each returns cudaGetLastError() after its launch.
+cudaError_t gdn_launch_prep(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
+cudaError_t gdn_launch_state(const gdn::LaunchCommon &p, int D, cudaStream_t st);
+cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
+cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *dst1, const void *src1,
+                            size_t bytes1, cudaStream_t st);
+cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);

@@ -269,3 +269,27 @@ WORKLOADS = {
 
 def grid_floor(n: int, c: int) -> int:
     return (n // c) * c
+
+
+# ---------------------------------------------------------------------------
+# Host arrays -> torch tensors (data movement only)
+# ---------------------------------------------------------------------------
+
+def to_torch(a: np.ndarray, dtype: str, device=None, pin: bool = False):
+    """Stored input values as a torch tensor (bf16 bits -> torch.bfloat16, else float32)."""
+    import torch
+    a = np.ascontiguousarray(a)
+    if dtype == BF16 and a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a.astype(np.float32, copy=False))
+    if pin:
+        t = t.pin_memory()
+    return t.to(device) if device is not None else t
+
+
+def tokens_to_torch(tok: Tokens, dtype: str, device=None, pin: bool = False):
+    """(xq, xk, xv, g, beta) as torch tensors."""
+    return (to_torch(tok.xq, dtype, device, pin), to_torch(tok.xk, dtype, device, pin),
+            to_torch(tok.xv, dtype, device, pin), to_torch(tok.g, FP32, device, pin),
+            to_torch(tok.beta, FP32, device, pin))

@@ -1,0 +1,181 @@
+/*
+ * gdn.h - C ABI of the GB300 (sm_103a) chunked Gated-DeltaNet prefill library.
+ *
+ * One hybrid Qwen3.5-style Gated-DeltaNet (GDN) layer. Per v-head h, reading
+ * q/k head h / (Hv/Hk), the layer
+ *   1. applies a causal short convolution (kernel 4) to each q, k and v
+ *      channel, with the last three raw inputs carried as the conv state;
+ *   2. L2-normalises q and k per head;
+ *   3. runs the gated delta rule
+ *        S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *        o_t = S_t q_t,
+ *      in chunked (WY / UT) form on 64-token blocks.
+ * Sources: the layer's state is the per-session "Gated-DeltaNet state"
+ * ("The shadow reader", section "One session's state"); a captured state holds
+ * the fp32 recurrent state and the last three conv inputs ("qwen3_5: run
+ * prompts that share prefixes once per prefix", section "Purpose"); the state
+ * advances only in whole grid chunks at absolute positions c * C, with the
+ * sub-grid tail pending and forks that restore the state ("The shadow reader",
+ * section "Exact on a grid").
+ *
+ * Conventions for every call:
+ *  - All pointers to tensors are DEVICE pointers (cudaMalloc / PyTorch CUDA
+ *    memory) unless stated otherwise, 16-byte aligned, C-contiguous. The
+ *    caller owns every buffer; the library allocates no device memory.
+ *  - Every call validates all arguments on the host before any device work. On
+ *    an error status nothing (device memory or host structs) has been changed.
+ *  - Device work is enqueued on `stream` and is asynchronous: a call returning
+ *    GDN_OK means the work was launched. GDN_ERR_CUDA reports a failed launch;
+ *    in that case state buffers may be partially written.
+ *  - Results are deterministic. A session's state after a sequence of on-grid
+ *    calls depends only on the token values and the grid, not on how the
+ *    tokens were split into calls, nor on which other sessions share a call.
+ *  - gdn_last_error() returns a message for the last failing call on the
+ *    calling host thread.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t). NULL means the legacy default stream. */
+typedef struct CUstream_st *gdn_stream_t;
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, bad flag, negative size */
+    GDN_ERR_SHAPE = 2,          /* unsupported head count, head dim, grid, dtype */
+    GDN_ERR_OFF_GRID = 3,       /* on-grid call on a session whose committed length is off grid */
+    GDN_ERR_STATE_MISMATCH = 4, /* session / slot belongs to another layer description, or slot is missing */
+    GDN_ERR_WORKSPACE = 5,      /* workspace too small */
+    GDN_ERR_CUDA = 6,           /* a CUDA call or launch failed */
+    GDN_ERR_TIMEOUT = 7         /* reserved for bounded device waits */
+} gdn_status;
+
+enum { GDN_FP32 = 0, GDN_BF16 = 1 };
+enum { GDN_CONV_NONE = 0, GDN_CONV_SILU = 1 };
+
+/* Flag of the prefill calls: also process the final partial grid chunk. */
+#define GDN_ALLOW_PARTIAL 1u
+
+/* Maximum sessions in one varlen / decode call. */
+#define GDN_MAX_SESSIONS 4096
+
+/* The layer. ch = 2 * n_qk_heads * d_k + n_v_heads * d_v conv channels, in the
+ * order q | k | v. */
+typedef struct gdn_layer_desc {
+    int32_t n_qk_heads; /* Hk >= 1 */
+    int32_t n_v_heads;  /* Hv, a multiple of Hk (GQA: v-head h reads q/k head h / (Hv/Hk)) */
+    int32_t d_k;        /* 64 or 128 */
+    int32_t d_v;        /* equal to d_k */
+    int32_t grid_c;     /* commit grid C: a multiple of 64 in [64, 4096] (the pages use 64 and 512) */
+    int32_t in_dtype;   /* GDN_BF16 or GDN_FP32: x_q, x_k, x_v, conv weights and conv state */
+    int32_t out_dtype;  /* GDN_FP32 or GDN_BF16 */
+    int32_t conv_act;   /* GDN_CONV_NONE (default) or GDN_CONV_SILU after the conv */
+    float q_scale;      /* multiplies the normalised q (1.0) */
+    float l2_eps;       /* added to |y|^2 inside the square root of the L2 norm (1e-6), > 0 */
+} gdn_layer_desc;
+
+/* A session's recurrent state, or a checkpoint slot (same layout).
+ * Host struct; S and conv point to caller-owned device memory. */
+typedef struct gdn_session {
+    float *S;          /* fp32 [Hv][d_k][d_v]: the state S transposed (row = key dim) */
+    void *conv;        /* in_dtype [3][ch]: raw inputs of the last three positions, oldest first */
+    int64_t committed; /* tokens consumed so far = absolute position of the next token; -1 = missing slot */
+    uint64_t tag;      /* gdn_desc_tag() of the layer this state belongs to */
+} gdn_session;
+
+/* Hash of every field of the description; sessions and slots carry it and
+ * calls refuse a state whose tag differs (another layer, grid or format). */
+uint64_t gdn_desc_tag(const gdn_layer_desc *desc);
+
+/* GDN_OK if the description is supported. */
+gdn_status gdn_desc_check(const gdn_layer_desc *desc);
+
+/* Bytes of S and of the conv state for one session of this layer (0 if invalid). */
+size_t gdn_state_bytes(const gdn_layer_desc *desc);
+size_t gdn_conv_state_bytes(const gdn_layer_desc *desc);
+
+/* Binds S and conv (device buffers of gdn_state_bytes / gdn_conv_state_bytes)
+ * to *session, zeroes them on `stream`, sets committed = 0 and the tag. */
+gdn_status gdn_session_init(const gdn_layer_desc *desc, gdn_session *session, float *S,
+                            void *conv, gdn_stream_t stream);
+
+/* Workspace bytes a prefill call needs for up to `max_tokens` tokens in total
+ * over up to `max_sessions` sessions. Scratch of one call: its contents are
+ * not needed afterwards, and calls that overlap on the GPU must not share it. */
+size_t gdn_workspace_size(const gdn_layer_desc *desc, int64_t max_tokens, int32_t max_sessions);
+
+/* Prefill of one session.
+ *   xq, xk: in_dtype [n_tokens][Hk * d_k]; xv: in_dtype [n_tokens][Hv * d_v];
+ *   g: fp32 [n_tokens][Hv] log-decay (g <= 0); beta: fp32 [n_tokens][Hv];
+ *   conv_w: in_dtype [ch][4], tap 3 multiplies the current token;
+ *   out: out_dtype [n_tokens][Hv][d_v].
+ * Without GDN_ALLOW_PARTIAL the session must be on grid (committed % C == 0)
+ * and the call consumes the largest multiple of C of the given tokens; the
+ * rest (< C) is the pending tail, which the caller keeps and sends again with
+ * the next call. With GDN_ALLOW_PARTIAL every token is consumed, the last grid
+ * chunk may be partial and the session may be left off grid: the next call on
+ * it must be another partial call, a decode step or a restore.
+ * Rows of `out` for consumed tokens are written; the others are untouched.
+ * *n_consumed (host) receives the consumed count; session->committed grows by it. */
+gdn_status gdn_prefill_chunks(const gdn_layer_desc *desc, gdn_session *session, const void *xq,
+                              const void *xk, const void *xv, const float *g, const float *beta,
+                              const void *conv_w, int64_t n_tokens, uint32_t flags, void *out,
+                              int64_t *n_consumed, void *workspace, size_t workspace_bytes,
+                              gdn_stream_t stream);
+
+/* Prefill of n_sessions sessions in one pass (packed / varlen batch).
+ * Session i's tokens are rows [cu_seqlens[i], cu_seqlens[i+1]) of the packed
+ * xq, xk, xv, g, beta and out (same per-row layouts as gdn_prefill_chunks).
+ * cu_seqlens is a HOST array of n_sessions + 1 non-decreasing offsets starting
+ * at 0. The sessions must be distinct. Each session follows the rules of
+ * gdn_prefill_chunks; n_consumed (host) has n_sessions entries. Every session's
+ * result is bit-identical to a gdn_prefill_chunks call on it alone. */
+gdn_status gdn_prefill_varlen(const gdn_layer_desc *desc, gdn_session *sessions, int32_t n_sessions,
+                              const int64_t *cu_seqlens, const void *xq, const void *xk,
+                              const void *xv, const float *g, const float *beta,
+                              const void *conv_w, uint32_t flags, void *out, int64_t *n_consumed,
+                              void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
+/* Checkpoint: bitwise copy of src's S and conv state into slot (device to
+ * device), and of its committed length and tag. The slot is marked missing
+ * (committed = -1) first and only filled in when the copy was launched, so a
+ * failed capture leaves a missing slot, never a stale one ("Long context and
+ * sessions", section "Checkpoints"; saveSlot in "Sessions on one engine"). */
+gdn_status gdn_state_capture(const gdn_layer_desc *desc, const gdn_session *src, gdn_session *slot,
+                             gdn_stream_t stream);
+
+/* Puts a captured state back: bitwise copy of slot into dst (S, conv,
+ * committed). Refuses a missing slot or one of another layer description. */
+gdn_status gdn_state_restore(const gdn_layer_desc *desc, gdn_session *dst, const gdn_session *slot,
+                             gdn_stream_t stream);
+
+/* Copies the session's conv state (in_dtype [3][ch], oldest row first) to
+ * `out`, which may be device memory or pinned host memory. */
+gdn_status gdn_conv_state(const gdn_layer_desc *desc, const gdn_session *session, void *out,
+                          gdn_stream_t stream);
+
+/* One token for each of n_sessions sessions (a decode step; leaves sessions
+ * off grid). Row i of xq, xk ([n][Hk*d_k]), xv ([n][Hv*d_v]), g, beta ([n][Hv])
+ * and out ([n][Hv][d_v]) belongs to sessions[i]; committed grows by one. */
+gdn_status gdn_decode_step(const gdn_layer_desc *desc, gdn_session *sessions, int32_t n_sessions,
+                           const void *xq, const void *xk, const void *xv, const float *g,
+                           const float *beta, const void *conv_w, void *out, gdn_stream_t stream);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char *gdn_last_error(void);
+
+/* Name of a status code. */
+const char *gdn_status_string(gdn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

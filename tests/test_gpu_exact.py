@@ -1,0 +1,238 @@
+"""Bit-exact GPU-vs-GPU checks of the grid, fork, shared-prefix and batching rules.
+
+* on-grid replay (turn by turn, sub-grid tail held pending) equals a fresh
+  prefill on the same grid in every committed output row, the recurrent state
+  and the conv state ("The shadow reader", section "Exact on a grid");
+* a fork (capture, prefill tail + question with the partial flag, restore)
+  leaves the committed state unchanged, and its outputs equal a full pass;
+* shared prefixes cut at their last multiple of 64 and continued per branch
+  equal a full-prompt pass ("qwen3_5: run prompts that share prefixes once per
+  prefix", sections "Purpose" and "Test Plan");
+* a session's result does not depend on the other sessions of a varlen call,
+  nor on sessions time-shared through checkpoint slots ("Long context and
+  sessions", section "Sessions on one engine").
+"""
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_deltanet_gb300 import gdn
+from chunked_gated_deltanet_gb300 import workloads as wl
+from helpers import Runner, desc_of
+
+pytestmark = pytest.mark.gpu
+
+
+def _same(a: torch.Tensor, b: torch.Tensor) -> bool:
+    torch.cuda.synchronize()
+    return torch.equal(a.view(torch.uint8) if a.dtype != torch.uint8 else a,
+                       b.view(torch.uint8) if b.dtype != torch.uint8 else b)
+
+
+def _replay(run: Runner, turns, out):
+    """Feed turns; each call sends the pending tail plus the turn's tokens."""
+    sess = run.session()
+    end = 0
+    for n in turns:
+        end += n
+        consumed = run.prefill(sess, sess.committed, end, out)
+        assert consumed % run.shape.grid_c == 0
+    return sess
+
+
+@pytest.mark.parametrize("C", [64, 512])
+def test_replay_equals_fresh(cuda_device, C):
+    shape = wl.Shape(2, 4, 128, 128, C, wl.BF16)
+    T = 5000
+    w = wl.Workload("replay", shape, seed=1, session_lengths=[T])
+    run = Runner(shape, w.session_tokens(0), w.conv_weights(), cuda_device)
+    turns = wl.split_turns(T, 9, np.random.default_rng(3))
+    o1, o2 = run.new_out(), run.new_out()
+    s1 = _replay(run, turns, o1)
+    s2 = run.session()
+    n = run.prefill(s2, 0, T, o2)
+    assert s1.committed == s2.committed == n == (T // C) * C
+    assert _same(o1[:n], o2[:n]) and _same(s1.S, s2.S) and _same(s1.conv, s2.conv)
+
+
+def test_grid64_equals_grid512_at_multiples_of_512(cuda_device):
+    T = 3072
+    w = wl.Workload("grids", wl.Shape(2, 2, 128, 128, 64, wl.BF16), seed=2, session_lengths=[T])
+    tok, cw = w.session_tokens(0), w.conv_weights()
+    r64 = Runner(wl.Shape(2, 2, 128, 128, 64, wl.BF16), tok, cw, cuda_device)
+    r512 = Runner(wl.Shape(2, 2, 128, 128, 512, wl.BF16), tok, cw, cuda_device)
+    o64, o512 = r64.new_out(), r512.new_out()
+    s64 = _replay(r64, [700, 64, 1000, 1308], o64)
+    s512 = _replay(r512, [1100, 1972], o512)
+    assert s64.committed == s512.committed == T
+    assert _same(o64, o512) and _same(s64.S, s512.S) and _same(s64.conv, s512.conv)
+
+
+def test_fork_restores_and_matches_full_pass(cuda_device):
+    shape = wl.Shape(2, 4, 128, 128, 512, wl.BF16)
+    T, Q = 2700, 150
+    w = wl.Workload("fork", shape, seed=4, session_lengths=[T])
+    tok, cw = w.session_tokens(0), w.conv_weights()
+    full = wl.Tokens.concat([tok, w.extra_tokens(0, Q)])
+    run = Runner(shape, full, cw, cuda_device)
+    out = run.new_out()
+    sess = run.session()
+    assert run.prefill(sess, 0, T, out) == 2560
+    S0, conv0 = sess.S.clone(), sess.conv.clone()
+    slot = run.session()
+    gdn.gdn_state_capture(run.desc, sess, slot)
+    # fork: pending tail (140) + question (150), partial allowed, then put the state back
+    assert run.prefill(sess, 2560, T + Q, out, gdn.GDN_ALLOW_PARTIAL) == T + Q - 2560
+    assert sess.committed == T + Q
+    with pytest.raises(gdn.GdnError) as e:           # off grid now: on-grid calls are refused
+        run.prefill(sess, T + Q, T + Q, out)
+    assert e.value.status == gdn.GDN_ERR_OFF_GRID
+    gdn.gdn_state_restore(run.desc, sess, slot)
+    assert sess.committed == 2560
+    assert _same(sess.S, S0) and _same(sess.conv, conv0)
+    # full pass of (session + question)
+    ref = run.session()
+    oref = run.new_out()
+    assert run.prefill(ref, 0, T + Q, oref, gdn.GDN_ALLOW_PARTIAL) == T + Q
+    assert _same(out, oref)
+
+
+def test_varlen_equals_solo(cuda_device):
+    shape = wl.Shape(2, 4, 128, 128, 512, wl.BF16)
+    lens = [1500, 513, 2100, 300]
+    w = wl.Workload("vl", shape, seed=6, session_lengths=lens)
+    cw = w.conv_weights()
+    toks = [w.session_tokens(i) for i in range(len(lens))]
+    packed = wl.Tokens.concat(toks)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    for flags in (0, gdn.GDN_ALLOW_PARTIAL):
+        run = Runner(shape, packed, cw, cuda_device)
+        sess = [run.session() for _ in lens]
+        out = run.new_out()
+        ws = gdn.workspace(run.desc, int(cu[-1]), len(lens), cuda_device)
+        nc = gdn.gdn_prefill_varlen(run.desc, sess, cu, *run.x, run.cw_t, out, ws, flags=flags)
+        for i, L in enumerate(lens):
+            solo = Runner(shape, toks[i], cw, cuda_device)
+            s, o = solo.session(), solo.new_out()
+            n = solo.prefill(s, 0, L, o, flags)
+            assert n == nc[i] == sess[i].committed
+            assert _same(out[cu[i]:cu[i] + n], o[:n])
+            assert _same(s.S, sess[i].S) and _same(s.conv, sess[i].conv)
+
+
+def test_interleaved_sessions_through_slots(cuda_device):
+    """One working session time-shared by 3 conversations through slots equals uninterrupted runs."""
+    shape = wl.Shape(2, 2, 128, 128, 64, wl.BF16)
+    lens = [900, 700, 1000]
+    w = wl.Workload("inter", shape, seed=8, session_lengths=lens)
+    cw = w.conv_weights()
+    runs = [Runner(shape, w.session_tokens(i), cw, cuda_device) for i in range(3)]
+    turns = [wl.split_turns(L, 4, np.random.default_rng(10 + i)) for i, L in enumerate(lens)]
+    work = runs[0].session()
+    slots = [runs[0].session() for _ in range(3)]
+    outs = [r.new_out() for r in runs]
+    ends = [0, 0, 0]
+    for k in range(4):
+        for i in range(3):
+            gdn.gdn_state_restore(runs[i].desc, work, slots[i])
+            ends[i] += turns[i][k]
+            runs[i].prefill(work, work.committed, ends[i], outs[i])
+            gdn.gdn_state_capture(runs[i].desc, work, slots[i])
+    for i in range(3):
+        s, o = runs[i].session(), runs[i].new_out()
+        n = runs[i].prefill(s, 0, lens[i], o)
+        assert slots[i].committed == n
+        assert _same(outs[i][:n], o[:n]) and _same(slots[i].S, s.S) and _same(slots[i].conv, s.conv)
+
+
+def test_refused_requests_change_nothing(cuda_device):
+    shape = wl.Shape(2, 2, 128, 128, 512, wl.BF16)
+    w = wl.Workload("refuse", shape, seed=12, session_lengths=[2048])
+    run = Runner(shape, w.session_tokens(0), w.conv_weights(), cuda_device)
+    a, b = run.session(), run.session()
+    oa, ob = run.new_out(), run.new_out()
+    run.prefill(a, 0, 1024, oa)
+    run.prefill(b, 0, 1024, ob)
+    S_before = b.S.clone()
+    small_ws = torch.empty(1024, dtype=torch.uint8, device=cuda_device)
+    xq, xk, xv, g, beta = (t[1024:] for t in run.x)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_prefill_chunks(run.desc, b, xq, xk, xv, g, beta, run.cw_t, ob[1024:], small_ws)
+    assert e.value.status == gdn.GDN_ERR_WORKSPACE
+    other = desc_of(wl.Shape(2, 2, 128, 128, 64, wl.BF16))
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_prefill_chunks(other, b, xq, xk, xv, g, beta, run.cw_t, ob[1024:], run.ws)
+    assert e.value.status == gdn.GDN_ERR_STATE_MISMATCH
+    assert b.committed == 1024 and _same(b.S, S_before)
+    run.prefill(a, 1024, 2048, oa)
+    run.prefill(b, 1024, 2048, ob)
+    assert _same(oa, ob) and _same(a.S, b.S) and _same(a.conv, b.conv)
+
+
+def _shared_prefix_run(w: wl.Workload, cw, device, reverse=False):
+    """Prefix runs once to its last multiple of 64; groups and branches continue from captured states."""
+    shape = w.shape
+    R = w.request_prefix
+    req = w.session_tokens(0, R)
+    groups = [w.extra_tokens(g, gp) for g, gp in enumerate(w.group_prefixes)]
+    res = {}
+    full_tok = wl.Tokens.concat([req] + groups + [w.extra_tokens(100 + 4 * g + b, n)
+                                                  for g, br in enumerate(w.branches) for b, n in enumerate(br)])
+    run = Runner(shape, full_tok, cw, device)
+    desc = run.desc
+    cut = wl.grid_floor(R, 64)
+    prefix_sess, prefix_slot = run.session(), run.session()
+    scratch = run.new_out(R)
+    xs = lambda toks: wl.tokens_to_torch(toks, shape.dtype, device)
+
+    def feed(sess, toks, a, b, out, flags):
+        x = xs(toks.slice(a, b))
+        return gdn.gdn_prefill_chunks(desc, sess, *x, run.cw_t, out, run.ws, flags=flags)
+
+    assert feed(prefix_sess, req, 0, cut, scratch, 0) == cut
+    gdn.gdn_state_capture(desc, prefix_sess, prefix_slot)
+    slot_copy = prefix_slot.S.clone()
+    g_order = list(range(len(w.group_prefixes)))
+    if reverse:
+        g_order.reverse()
+    work = run.session()
+    for g in g_order:
+        gp = w.group_prefixes[g]
+        prompt = wl.Tokens.concat([req, groups[g]])
+        gcut = wl.grid_floor(R + gp, 64)
+        gslot = run.session()
+        gdn.gdn_state_restore(desc, work, prefix_slot)
+        if gcut > cut:
+            assert feed(work, prompt, cut, gcut, run.new_out(gcut - cut), 0) == gcut - cut
+        gdn.gdn_state_capture(desc, work, gslot)
+        b_order = list(range(len(w.branches[g])))
+        if reverse:
+            b_order.reverse()
+        for b in b_order:
+            n = w.branches[g][b]
+            bt = wl.Tokens.concat([prompt, w.extra_tokens(100 + 4 * g + b, n)])
+            gdn.gdn_state_restore(desc, work, gslot)
+            ob = run.new_out(len(bt) - gcut)
+            assert feed(work, bt, gcut, len(bt), ob, gdn.GDN_ALLOW_PARTIAL) == len(bt) - gcut
+            res[(g, b)] = (bt, gcut, ob, work.S.clone(), work.conv.clone())
+    assert _same(prefix_slot.S, slot_copy) and prefix_slot.committed == cut
+    return run, res
+
+
+def test_shared_prefix_branches_equal_full_pass(cuda_device):
+    """Request prefix 1,000; groups 0/1/70/128; 4 branches each; grid 64."""
+    w = wl.shared_prefix()
+    cw = w.conv_weights()
+    run, res = _shared_prefix_run(w, cw, cuda_device)
+    assert len(res) == 16
+    for (g, b), (bt, gcut, ob, S, conv) in res.items():
+        x = wl.tokens_to_torch(bt, w.shape.dtype, cuda_device)
+        sess = run.session()
+        of = run.new_out(len(bt))
+        assert gdn.gdn_prefill_chunks(run.desc, sess, *x, run.cw_t, of, run.ws, flags=gdn.GDN_ALLOW_PARTIAL) == len(bt)
+        assert _same(ob, of[gcut:]), (g, b)
+        assert _same(S, sess.S) and _same(conv, sess.conv)
+    # state isolation: groups and branches reversed give the same results
+    _, res2 = _shared_prefix_run(w, cw, cuda_device, reverse=True)
+    for k, v in res.items():
+        assert _same(v[2], res2[k][2]) and _same(v[3], res2[k][3])
