@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Benchmark: chunked Gated-DeltaNet prefill tokens/s per layer on one GB300.
+
+Default workload: the Qwen3.5-0.8B-shaped layer (16 heads, d_k = d_v = 128,
+grid C = 512, bf16 inputs, fp32 state and outputs), one session of 41,802
+synthetic tokens fed as 30 turns of 200..4,000 tokens with the sub-grid tail
+held pending, a checkpoint captured at every turn end (6 rotating slots), and
+at the end one fork that prefills the 330-token pending tail plus a 290-token
+question and restores the state ("The shadow reader", sections "One session's
+state", "Exact on a grid" and "Who asks"). One step = that whole sequence.
+
+Prints one JSON line. `value` = tokens processed per second with inputs
+resident in HBM (CUDA events on the launching stream, K timed steps after W
+warm-ups); `e2e` = the same with inputs copied from pinned host memory and the
+outputs copied back inside the timed region; `roofline` = the dominant
+kernel's achieved HBM bandwidth (algorithmic bytes / average launch time)
+against the measured copy peak; `cpu_baseline` = the fp64 oracle on the host
+cores over a bounded sample of the same workload.
+
+`--impl reference` times the oracle itself (the reference arm of this method).
+Several GPUs run independent replicas (the layer needs no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s per layer on 1 GB300 + % of tensor-pipe/HBM roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# Algorithmic HBM bytes per token of the fused layer: q and k per q/k head
+# (2 d_k inputs), v per v-head, the output per v-head, g and beta per v-head.
+def algorithmic_bytes_per_token(Hk, Hv, d, in_bytes, out_bytes):
+    return Hk * 2 * d * in_bytes + Hv * d * in_bytes + Hv * d * out_bytes + Hv * 8
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group("gloo")
+    return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_max_sum(ms: float, units: float):
+    """(max of ms, sum of units) over ranks; identity on one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return ms, units
+    t = torch.tensor([ms], dtype=torch.float64)
+    u = torch.tensor([units], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.3)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S")) + float("0." + f[0].split(".")[1])
+            except Exception:
+                ts = None
+            rows.append((ts, f))
+        inside = [f for ts, f in rows if ts is not None and self.t0 - 0.2 <= ts <= self.t1 + 0.2] or [f for _, f in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for f in inside for i in range(4) if f[6 + i].lower().startswith("active")})
+        sm = [float(f[2]) for f in inside if re.match(r"^[0-9.]+$", f[2])]
+        mx = [float(f[3]) for f in inside if re.match(r"^[0-9.]+$", f[3])]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# the workload step
+# ---------------------------------------------------------------------------
+
+class ReplayStep:
+    """30 turns with checkpoints, then one fork over the pending tail plus a question."""
+
+    def __init__(self, w, device):
+        import torch
+        from chunked_gated_deltanet_gb300 import gdn
+        from chunked_gated_deltanet_gb300 import workloads as wl
+        self.gdn, self.torch = gdn, torch
+        self.w = w
+        sh = w.shape
+        self.T = w.session_lengths[0]
+        self.Q = w.fork_questions[0]
+        tok = wl.Tokens.concat([w.session_tokens(0), w.extra_tokens(0, self.Q)])
+        self.rows = len(tok)
+        self.desc = gdn.make_desc(sh.n_qk_heads, sh.n_v_heads, sh.d_k, sh.d_v, sh.grid_c, gdn.GDN_BF16, gdn.GDN_FP32)
+        self.host = wl.tokens_to_torch(tok, sh.dtype, None, pin=True)
+        self.host_cw = wl.to_torch(w.conv_weights(), sh.dtype, None, pin=True)
+        self.x = [t.to(device) for t in self.host]
+        self.cw = self.host_cw.to(device)
+        self.out = torch.empty((self.rows, sh.n_v_heads, sh.d_v), dtype=torch.float32, device=device)
+        self.host_out = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        C = sh.grid_c
+        self.calls, end, committed = [], 0, 0
+        for n in w.turns[0]:
+            end += n
+            take = (end - committed) // C * C
+            self.calls.append((committed, end, take))
+            committed += take
+        self.committed = committed
+        self.fork = (committed, self.rows)
+        max_call = max([e - s for s, e, _ in self.calls] + [self.rows - committed])
+        self.ws = gdn.workspace(self.desc, max_call, 1, device)
+        self.sess = gdn.Session(self.desc, device)
+        self.slots = [gdn.Session(self.desc, device) for _ in range(w.n_slots)]
+        self.fork_slot = gdn.Session(self.desc, device)
+        self.tokens_per_step = committed + (self.rows - committed)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host) + \
+            self.host_cw.numel() * self.host_cw.element_size()
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+
+    def step(self):
+        g = self.gdn
+        d, s, x, cw, out, ws = self.desc, self.sess, self.x, self.cw, self.out, self.ws
+        g.gdn_session_init(d, s)
+        for k, (a, b, take) in enumerate(self.calls):
+            n = g.gdn_prefill_chunks(d, s, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b], cw, out[a:b], ws)
+            assert n == take
+            g.gdn_state_capture(d, s, self.slots[k % len(self.slots)])
+        g.gdn_state_capture(d, s, self.fork_slot)
+        a, b = self.fork
+        g.gdn_prefill_chunks(d, s, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b], cw, out[a:b], ws,
+                             flags=g.GDN_ALLOW_PARTIAL)
+        g.gdn_state_restore(d, s, self.fork_slot)
+
+    def e2e_step(self):
+        for dst, src in zip(self.x, self.host):
+            dst.copy_(src, non_blocking=True)
+        self.cw.copy_(self.host_cw, non_blocking=True)
+        self.step()
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def config(self):
+        sh = self.w.shape
+        return {"workload": self.w.name, "sessions": 1, "session_tokens": self.T, "turns": len(self.w.turns[0]),
+                "checkpoint_slots": len(self.slots), "fork_tokens": self.rows - self.committed,
+                "tokens_per_step": self.tokens_per_step, "n_qk_heads": sh.n_qk_heads, "n_v_heads": sh.n_v_heads,
+                "d_k": sh.d_k, "d_v": sh.d_v, "grid_c": sh.grid_c, "inputs": "bf16", "state": "fp32",
+                "outputs": "fp32",
+                "l2": f"inputs larger than L2 ({self.h2d_bytes / 1e6:.0f} MB read per step vs 129 MB L2)",
+                "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle over a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, n_tokens: int):
+    import numpy as np
+    import oracle
+    from chunked_gated_deltanet_gb300 import workloads as wl
+    tok = w.session_tokens(0).slice(0, n_tokens)
+    f = lambda a: wl.as_f64(a, w.shape.dtype)
+    args = (f(tok.xq), f(tok.xk), f(tok.xv), tok.g.astype(np.float64), tok.beta.astype(np.float64),
+            f(w.conv_weights()))
+    sh = w.shape
+
+    def run():
+        oracle.layer(*args, sh.n_qk_heads, sh.n_v_heads)
+
+    return run
+
+
+def cpu_threads(n_heads: int) -> int:
+    try:
+        c = len(os.sched_getaffinity(0))
+    except Exception:
+        c = os.cpu_count() or 1
+    return max(1, min(c, n_heads))
+
+
+def traffic_record(kernel_file: str):
+    """Per-token DRAM bytes of the dominant kernel from the committed ncu summary, if the kernel is unchanged."""
+    src = os.path.join(ROOT, "chunked_gated_deltanet_gb300", "csrc", kernel_file)
+    prof = os.path.join(ROOT, "profiles", "state_output_qwen08b_replay.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        txt = open(prof).read()
+        m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
+        m_b = re.search(r"dram_bytes_per_token:\s*([0-9.]+)", txt)
+        if m_sha and m_b and m_sha.group(1) == sha:
+            return float(m_b.group(1))
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=41472)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+
+    rank, world, local = _dist()
+    from chunked_gated_deltanet_gb300 import workloads as wl
+    w = wl.qwen08b_replay()
+
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+
+    import torch
+    from chunked_gated_deltanet_gb300 import gdn
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gdn.load_library()
+    step = ReplayStep(w, dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.step()
+    torch.cuda.synchronize()
+
+    # --- device-resident timed region ---
+    clk = ClockSampler(local)
+    clk.start()
+    barrier()
+    torch.cuda.synchronize()
+    gdn.gdn_timing_begin(100_000)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk.mark("t0")
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step.step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk.mark("t1")
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    ktimes = gdn.gdn_timing_end()
+    clocks = clk.stop()
+    ms_max, tokens_all = reduce_max_sum(ms, step.tokens_per_step * args.steps)
+    value = tokens_all / (ms_max / 1e3)
+
+    # --- end to end through host buffers ---
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(2):
+            step.e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step.e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems, etok = reduce_max_sum(e0.elapsed_time(e1), step.tokens_per_step * args.steps)
+        e2e = {"value": etok / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": step.h2d_bytes,
+               "d2h_bytes_per_step": step.d2h_bytes}
+
+    # --- roofline of the dominant kernel ---
+    sh = w.shape
+    bpt = algorithmic_bytes_per_token(sh.n_qk_heads, sh.n_v_heads, sh.d_k, 2, 4)
+    dom = max(ktimes.items(), key=lambda kv: kv[1][2])
+    name, (launches, timed, tot_ms) = dom
+    avg_ms = tot_ms / max(timed, 1)
+    # tokens one launch of the dominant kernel processes (prefill kernels: every consumed token of the step)
+    prefill_launches = launches / args.steps
+    tokens_per_launch = step.tokens_per_step / prefill_launches
+    achieved = bpt * tokens_per_launch / (avg_ms / 1e3) / 1e9
+    peak, peak_src = measured_peaks()
+    traffic_bpt = traffic_record("state.cu") if name == "state_output" else None
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_src, "kernel": name,
+                "algorithmic_bytes_per_token": bpt, "tokens_per_launch": round(tokens_per_launch, 1),
+                "avg_launch_ms": round(avg_ms, 4),
+                "traffic": round(traffic_bpt * tokens_per_launch) if traffic_bpt else None,
+                "step_frac": round(bpt * step.tokens_per_step / (ms / args.steps / 1e3) / 1e9 / peak, 4)}
+    kernels = {k: {"launches_per_step": v[0] / args.steps, "ms_per_step": round(v[2] / args.steps, 4),
+                   "share": round(v[2] / sum(x[2] for x in ktimes.values()), 4)} for k, v in ktimes.items()}
+    gpu_launches = int(sum(v[0] for v in ktimes.values()))
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": step.config(),
+            "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline, "kernels": kernels, "clocks": clocks}
+
+    # --- CPU baseline (oracle), rank 0 at N=1 only ---
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = min(args.cpu_sample_tokens, w.session_lengths[0])
+        run = oracle_sample(w, n)
+        t0 = time.time()
+        run()
+        dt = time.time() - t0
+        line["cpu_baseline"] = {"value": round(n / dt, 1), "unit": UNIT, "cores": cpu_threads(sh.n_v_heads),
+                                "kind": "oracle",
+                                "sample": f"first {n} tokens of the {w.session_lengths[0]}-token session, all "
+                                          f"{sh.n_v_heads} heads, one fp64 oracle call ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, w, rank, world):
+    """The oracle as the reference arm: rank 0 alone, host cores."""
+    if rank != 0:
+        return
+    n = min(args.cpu_sample_tokens, w.session_lengths[0])
+    run = oracle_sample(w, n)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.time()
+    for _ in range(args.steps):
+        run()
+    dt = time.time() - t0
+    v = n * args.steps / dt
+    sh = w.shape
+    cores = cpu_threads(sh.n_v_heads)
+    sample = (f"first {n} tokens of the {w.session_lengths[0]}-token session per step, all {sh.n_v_heads} heads, "
+              f"fp64 oracle")
+    line = {"metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample_tokens_per_step": n, "n_qk_heads": sh.n_qk_heads,
+                       "n_v_heads": sh.n_v_heads, "d_k": sh.d_k, "d_v": sh.d_v, "grid_c": sh.grid_c,
+                       "parallelism": "host threads over heads"},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

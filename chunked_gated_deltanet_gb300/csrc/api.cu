@@ -111,7 +111,85 @@ void fill_common(LaunchCommon &p, const gdn_layer_desc *d, const void *xq, const
     p.q_scale = d->q_scale; p.eps = d->l2_eps;
 }
 
+// ---- optional per-kernel event timing ----
+enum Kind { K_PREP = 0, K_CONV = 1, K_STATE = 2, K_COPY = 3, K_DECODE = 4, K_KINDS = 5 };
+const char *const kKindName[K_KINDS] = {"prep_wy", "conv_commit", "state_output", "state_copy", "decode"};
+
+struct Timing {
+    bool on = false;
+    int cap = 0, used = 0;
+    std::vector<cudaEvent_t> ev;  // 2 per timed launch
+    std::vector<int> kind;
+    int64_t launches[K_KINDS] = {};
+};
+Timing g_timing;
+
+template <class F>
+cudaError_t launch_k(Kind k, cudaStream_t st, F &&f) {
+    Timing &T = g_timing;
+    if (!T.on) return f();
+    T.launches[k]++;
+    if (T.used >= T.cap) return f();
+    cudaEvent_t a = T.ev[2 * T.used], b = T.ev[2 * T.used + 1];
+    cudaError_t e = cudaEventRecord(a, st);
+    if (e != cudaSuccess) return e;
+    e = f();
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(b, st);
+    if (e == cudaSuccess) T.kind[T.used++] = k;
+    return e;
+}
+
 }  // namespace
+
+GDN_API gdn_status gdn_timing_begin(int32_t max_launches) {
+    Timing &T = g_timing;
+    if (T.on) return fail(GDN_ERR_INVALID_ARG, "timing already recording");
+    if (max_launches < 0 || max_launches > (1 << 22)) return fail(GDN_ERR_INVALID_ARG, "max_launches out of range");
+    for (cudaEvent_t e : T.ev) cudaEventDestroy(e);
+    T.ev.assign(2 * (size_t)max_launches, nullptr);
+    for (auto &e : T.ev) {
+        cudaError_t r = cudaEventCreate(&e);
+        if (r != cudaSuccess) return cuda_fail(r, "event creation");
+    }
+    T.kind.assign(max_launches, 0);
+    T.cap = max_launches;
+    T.used = 0;
+    for (auto &l : T.launches) l = 0;
+    T.on = true;
+    return GDN_OK;
+}
+
+GDN_API gdn_status gdn_timing_end(gdn_kernel_time *out, int32_t max_kinds, int32_t *n_kinds) {
+    Timing &T = g_timing;
+    if (!T.on) return fail(GDN_ERR_INVALID_ARG, "timing is not recording");
+    T.on = false;
+    double ms[K_KINDS] = {};
+    int64_t timed[K_KINDS] = {};
+    for (int i = 0; i < T.used; ++i) {
+        cudaError_t r = cudaEventSynchronize(T.ev[2 * i + 1]);
+        if (r != cudaSuccess) return cuda_fail(r, "event wait");
+        float m = 0.f;
+        r = cudaEventElapsedTime(&m, T.ev[2 * i], T.ev[2 * i + 1]);
+        if (r != cudaSuccess) return cuda_fail(r, "event elapsed time");
+        ms[T.kind[i]] += m;
+        timed[T.kind[i]]++;
+    }
+    int n = 0;
+    for (int k = 0; k < K_KINDS; ++k) {
+        if (T.launches[k] == 0) continue;
+        if (out && n < max_kinds) {
+            std::memset(&out[n], 0, sizeof(out[n]));
+            snprintf(out[n].name, sizeof(out[n].name), "%s", kKindName[k]);
+            out[n].launches = T.launches[k];
+            out[n].timed = timed[k];
+            out[n].total_ms = ms[k];
+        }
+        ++n;
+    }
+    if (n_kinds) *n_kinds = n;
+    return GDN_OK;
+}
 
 GDN_API uint64_t gdn_desc_tag(const gdn_layer_desc *desc) {
     if (check_desc(desc) != GDN_OK) return 0;
@@ -137,8 +215,10 @@ GDN_API gdn_status gdn_session_init(const gdn_layer_desc *d, gdn_session *s, flo
     if (!s) return fail(GDN_ERR_INVALID_ARG, "session is NULL");
     if (!S || !conv || !aligned16(S) || !aligned16(conv))
         return fail(GDN_ERR_INVALID_ARG, "S and conv must be non-NULL and 16-byte aligned");
-    cudaError_t e = gdn_launch_copy(S, nullptr, gdn_state_bytes(d), conv, nullptr, gdn_conv_state_bytes(d),
-                                    (cudaStream_t)stream);
+    cudaError_t e = launch_k(K_COPY, (cudaStream_t)stream, [&] {
+        return gdn_launch_copy(S, nullptr, gdn_state_bytes(d), conv, nullptr, gdn_conv_state_bytes(d),
+                               (cudaStream_t)stream);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "session zeroing");
     s->S = S; s->conv = conv; s->committed = 0; s->tag = tag_of(d);
     return GDN_OK;
@@ -234,11 +314,11 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
             i0 = i;
             if (cnt == 0) continue;
             p.n_sess = cnt; p.nblk = blk;
-            cudaError_t e = gdn_launch_prep(p, D, in_bf16, ch, cst);
+            cudaError_t e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep(p, D, in_bf16, ch, cst); });
             if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
-            e = gdn_launch_conv_commit(p, D, in_bf16, ch, cst);
+            e = launch_k(K_CONV, cst, [&] { return gdn_launch_conv_commit(p, D, in_bf16, ch, cst); });
             if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
-            e = gdn_launch_state(p, D, cst);
+            e = launch_k(K_STATE, cst, [&] { return gdn_launch_state(p, D, cst); });
             if (e != cudaSuccess) return cuda_fail(e, "state/output kernel");
         }
     }
@@ -270,8 +350,10 @@ GDN_API gdn_status gdn_state_capture(const gdn_layer_desc *d, const gdn_session 
     if (slot->S == src->S) return fail(GDN_ERR_INVALID_ARG, "slot and source share their buffers");
     slot->committed = -1;  // missing until the copy is enqueued
     slot->tag = 0;
-    cudaError_t e = gdn_launch_copy(slot->S, src->S, gdn_state_bytes(d), slot->conv, src->conv,
-                                    gdn_conv_state_bytes(d), (cudaStream_t)stream);
+    cudaError_t e = launch_k(K_COPY, (cudaStream_t)stream, [&] {
+        return gdn_launch_copy(slot->S, src->S, gdn_state_bytes(d), slot->conv, src->conv,
+                               gdn_conv_state_bytes(d), (cudaStream_t)stream);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "state capture copy");
     slot->committed = src->committed;
     slot->tag = src->tag;
@@ -285,8 +367,10 @@ GDN_API gdn_status gdn_state_restore(const gdn_layer_desc *d, gdn_session *dst, 
     if ((st = check_state(d, slot, "slot", true)) != GDN_OK) return st;
     if ((st = check_state(d, dst, "destination session", false)) != GDN_OK) return st;
     if (slot->S == dst->S) return fail(GDN_ERR_INVALID_ARG, "slot and destination share their buffers");
-    cudaError_t e = gdn_launch_copy(dst->S, slot->S, gdn_state_bytes(d), dst->conv, slot->conv,
-                                    gdn_conv_state_bytes(d), (cudaStream_t)stream);
+    cudaError_t e = launch_k(K_COPY, (cudaStream_t)stream, [&] {
+        return gdn_launch_copy(dst->S, slot->S, gdn_state_bytes(d), dst->conv, slot->conv,
+                               gdn_conv_state_bytes(d), (cudaStream_t)stream);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "state restore copy");
     dst->committed = slot->committed;
     return GDN_OK;
@@ -340,9 +424,10 @@ GDN_API gdn_status gdn_decode_step(const gdn_layer_desc *d, gdn_session *session
             r.S = sessions[i0 + j].S; r.conv = sessions[i0 + j].conv;
         }
         p.n_sess = cnt; p.nblk = 0;
-        cudaError_t e = gdn_launch_decode(p, D, in_bf16, ch, (cudaStream_t)stream);
+        cudaStream_t cst = (cudaStream_t)stream;
+        cudaError_t e = launch_k(K_DECODE, cst, [&] { return gdn_launch_decode(p, D, in_bf16, ch, cst); });
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
-        e = gdn_launch_conv_commit(p, D, in_bf16, ch, (cudaStream_t)stream);
+        e = launch_k(K_CONV, cst, [&] { return gdn_launch_conv_commit(p, D, in_bf16, ch, cst); });
         if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
     }
     for (int i = 0; i < n; ++i) sessions[i].committed += 1;

@@ -32,7 +32,8 @@ GDN_MAX_SESSIONS = 4096
 
 EXPORTED = ["gdn_desc_tag", "gdn_desc_check", "gdn_state_bytes", "gdn_conv_state_bytes", "gdn_session_init",
             "gdn_workspace_size", "gdn_prefill_chunks", "gdn_prefill_varlen", "gdn_state_capture",
-            "gdn_state_restore", "gdn_conv_state", "gdn_decode_step", "gdn_last_error", "gdn_status_string"]
+            "gdn_state_restore", "gdn_conv_state", "gdn_decode_step", "gdn_timing_begin", "gdn_timing_end",
+            "gdn_last_error", "gdn_status_string"]
 
 
 class gdn_layer_desc(ctypes.Structure):
@@ -45,6 +46,11 @@ class gdn_layer_desc(ctypes.Structure):
 class gdn_session(ctypes.Structure):
     _fields_ = [("S", ctypes.c_void_p), ("conv", ctypes.c_void_p), ("committed", ctypes.c_int64),
                 ("tag", ctypes.c_uint64)]
+
+
+class gdn_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int64), ("timed", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
 
 
 class GdnError(RuntimeError):
@@ -84,6 +90,8 @@ def load_library(path: Optional[str] = None):
         "gdn_state_restore": (ctypes.c_int, [D, Sp, Sp, vp]),
         "gdn_conv_state": (ctypes.c_int, [D, Sp, vp, vp]),
         "gdn_decode_step": (ctypes.c_int, [D, Sp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
+        "gdn_timing_begin": (ctypes.c_int, [i32]),
+        "gdn_timing_end": (ctypes.c_int, [ctypes.POINTER(gdn_kernel_time), i32, ctypes.POINTER(i32)]),
         "gdn_last_error": (ctypes.c_char_p, []),
         "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
@@ -236,3 +244,16 @@ def gdn_decode_step(desc, sessions: Sequence[Session], xq, xk, xv, g, beta, conv
     for i, s in enumerate(sessions):
         s.c.committed = arr[i].committed
     _check(st)
+
+
+def gdn_timing_begin(max_launches: int):
+    _check(load_library().gdn_timing_begin(max_launches))
+
+
+def gdn_timing_end() -> dict:
+    """{kind: (launches, timed launches, total device ms)} since gdn_timing_begin."""
+    arr = (gdn_kernel_time * 8)()
+    n = ctypes.c_int32(0)
+    _check(load_library().gdn_timing_end(arr, 8, ctypes.byref(n)))
+    return {arr[i].name.decode(): (int(arr[i].launches), int(arr[i].timed), float(arr[i].total_ms))
+            for i in range(min(n.value, 8))}

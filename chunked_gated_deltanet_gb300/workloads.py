@@ -45,9 +45,15 @@ _ROW_CHUNK = 8192  # rows drawn per numpy call; draws are sequential, so chunkin
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 values to bf16 (round to nearest, ties to even); returns uint16 bit patterns."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    lsb = (b >> np.uint64(16)) & np.uint64(1)
-    r = (b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
+    if not np.isfinite(x).all():
+        raise ValueError("bf16 rounding of non-finite values is not supported")
+    b = x.view(np.uint32)
+    # finite values have bits <= 0xFF7FFFFF, so adding at most 0x8000 stays inside uint32
+    r = b >> np.uint32(16)
+    r &= np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += b
+    r >>= np.uint32(16)
     return r.astype(np.uint16)
 
 
@@ -64,7 +70,14 @@ def as_f64(arr: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def _round(x32: np.ndarray, dtype: str) -> np.ndarray:
-    return f32_to_bf16_bits(x32) if dtype == BF16 else np.ascontiguousarray(x32, dtype=np.float32)
+    if dtype != BF16:
+        return np.ascontiguousarray(x32, dtype=np.float32)
+    try:   # torch's float32 -> bfloat16 cast is round-to-nearest-even too, and vectorised
+        import torch
+        t = torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.bfloat16)
+        return t.view(torch.int16).numpy().view(np.uint16)
+    except ImportError:
+        return f32_to_bf16_bits(x32)
 
 
 def _sigmoid(x):

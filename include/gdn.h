@@ -168,6 +168,25 @@ gdn_status gdn_decode_step(const gdn_layer_desc *desc, gdn_session *sessions, in
                            const void *xq, const void *xk, const void *xv, const float *g,
                            const float *beta, const void *conv_w, void *out, gdn_stream_t stream);
 
+/* Per-kernel timing with CUDA events, for benchmarks (off by default).
+ * gdn_timing_begin(max_launches) creates 2 * max_launches events and starts
+ * recording: every kernel the library launches afterwards, on whatever stream
+ * the call names, is bracketed by an event pair on that stream (launches past
+ * max_launches are counted but not timed). gdn_timing_end waits for the
+ * recorded events, stops recording, and writes per kernel kind its launch
+ * count, timed launches and summed device milliseconds into out[0..max_kinds),
+ * with *n_kinds the number of kinds that launched. Process-global and not
+ * thread-safe: one benchmark thread at a time. */
+typedef struct gdn_kernel_time {
+    char name[32];        /* kernel kind: prep_wy, conv_commit, state_output, state_copy, decode */
+    int64_t launches;     /* launches while recording */
+    int64_t timed;        /* launches with an event pair */
+    double total_ms;      /* summed device time of the timed launches */
+} gdn_kernel_time;
+
+gdn_status gdn_timing_begin(int32_t max_launches);
+gdn_status gdn_timing_end(gdn_kernel_time *out, int32_t max_kinds, int32_t *n_kinds);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char *gdn_last_error(void);
 

@@ -69,3 +69,9 @@ def test_bf16_rounding_is_nearest_even():
     import torch
     ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
     assert np.array_equal(back[:5], ref[:5])
+
+
+def test_fast_bf16_path_equals_bit_formula():
+    rng = np.random.default_rng(0)
+    x = (rng.standard_normal(200_000) * np.exp(rng.uniform(-20, 20, 200_000))).astype(np.float32)
+    assert np.array_equal(wl._round(x, wl.BF16), wl.f32_to_bf16_bits(x))
