@@ -191,6 +191,8 @@ GDN_API gdn_status gdn_timing_end(gdn_kernel_time *out, int32_t max_kinds, int32
     return GDN_OK;
 }
 
+void gdn_internal_set_error(const char *msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 GDN_API uint64_t gdn_desc_tag(const gdn_layer_desc *desc) {
     if (check_desc(desc) != GDN_OK) return 0;
     return tag_of(desc);

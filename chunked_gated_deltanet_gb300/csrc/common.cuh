@@ -63,6 +63,9 @@ __device__ __forceinline__ float conv_tap(const float w[4], float xm3, float xm2
 
 }  // namespace gdn
 
+// Sets the message gdn_last_error() returns on this host thread (library-internal).
+void gdn_internal_set_error(const char *msg);
+
 // Launchers (host). Each returns cudaGetLastError() after its launch.
 cudaError_t gdn_launch_prep(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_state(const gdn::LaunchCommon &p, int D, cudaStream_t st);

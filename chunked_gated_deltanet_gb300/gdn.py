@@ -33,6 +33,7 @@ GDN_MAX_SESSIONS = 4096
 EXPORTED = ["gdn_desc_tag", "gdn_desc_check", "gdn_state_bytes", "gdn_conv_state_bytes", "gdn_session_init",
             "gdn_workspace_size", "gdn_prefill_chunks", "gdn_prefill_varlen", "gdn_state_capture",
             "gdn_state_restore", "gdn_conv_state", "gdn_decode_step", "gdn_timing_begin", "gdn_timing_end",
+            "gdn_prefill_chunks_noalloc",
             "gdn_last_error", "gdn_status_string"]
 
 
@@ -86,6 +87,7 @@ def load_library(path: Optional[str] = None):
                                               ctypes.c_size_t, vp]),
         "gdn_prefill_varlen": (ctypes.c_int, [D, Sp, i32, I64p, vp, vp, vp, vp, vp, vp, u32, vp, I64p, vp,
                                               ctypes.c_size_t, vp]),
+        "gdn_prefill_chunks_noalloc": (ctypes.c_int, [D, Sp, vp, vp, vp, vp, vp, vp, i64, u32, vp, I64p, vp]),
         "gdn_state_capture": (ctypes.c_int, [D, Sp, Sp, vp]),
         "gdn_state_restore": (ctypes.c_int, [D, Sp, Sp, vp]),
         "gdn_conv_state": (ctypes.c_int, [D, Sp, vp, vp]),
@@ -203,6 +205,20 @@ def gdn_prefill_chunks(desc, sess: Session, xq, xk, xv, g, beta, conv_w, out, ws
         ctypes.byref(desc), ctypes.byref(sess.c), _ptr(xq), _ptr(xk), _ptr(xv), _ptr(g), _ptr(beta),
         _ptr(conv_w), n, flags, _ptr(out), ctypes.byref(nc), _ptr(ws), ws.numel() if ws is not None else 0,
         _stream(stream)))
+    return int(nc.value)
+
+
+GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def gdn_prefill_chunks_noalloc(desc, sess: Session, xq, xk, xv, g, beta, conv_w, out, flags: int = 0,
+                               n_tokens: Optional[int] = None, stream=None) -> int:
+    """gdn_prefill_chunks with the library's built-in scratch (no workspace argument, no allocation)."""
+    n = int(g.shape[0]) if n_tokens is None else int(n_tokens)
+    nc = ctypes.c_int64(0)
+    _check(load_library().gdn_prefill_chunks_noalloc(
+        ctypes.byref(desc), ctypes.byref(sess.c), _ptr(xq), _ptr(xk), _ptr(xv), _ptr(g), _ptr(beta),
+        _ptr(conv_w), n, flags, _ptr(out), ctypes.byref(nc), _stream(stream)))
     return int(nc.value)
 
 

@@ -143,6 +143,31 @@ gdn_status gdn_prefill_varlen(const gdn_layer_desc *desc, gdn_session *sessions,
                               const void *conv_w, uint32_t flags, void *out, int64_t *n_consumed,
                               void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/* Bytes of the library's built-in scratch used by gdn_prefill_chunks_noalloc
+ * (held on every GPU that loads the library, until the process exits). */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* gdn_prefill_chunks for callers that cannot allocate device memory. The
+ * pages have no counterpart of this call; it exists for code whose device
+ * memory is planned up front by a host framework that owns the allocator, and
+ * for latency-critical callers that must not call cudaMalloc / cudaFree (those
+ * calls can synchronise the device). Arguments and results are those of
+ * gdn_prefill_chunks without the workspace: the scratch is a fixed
+ * GDN_NOALLOC_SCRATCH_BYTES array inside the library, and the call allocates
+ * nothing. A call whose processed tokens need more than that
+ * (gdn_workspace_size(desc, tokens processed, 1) > GDN_NOALLOC_SCRATCH_BYTES;
+ * about 830 tokens for 16 heads of d = 128) is refused with GDN_ERR_WORKSPACE
+ * before any device work. The first call on a device looks up the scratch's
+ * device address (cudaGetSymbolAddress) with that device current: make that
+ * first call before any stream capture. All calls in the process share the
+ * one scratch per device, so calls that overlap on the GPU (different streams
+ * without ordering between them) race and give wrong results; serialise them.
+ * No scratch content needs clearing between calls. */
+gdn_status gdn_prefill_chunks_noalloc(const gdn_layer_desc *desc, gdn_session *session, const void *xq,
+                                      const void *xk, const void *xv, const float *g, const float *beta,
+                                      const void *conv_w, int64_t n_tokens, uint32_t flags, void *out,
+                                      int64_t *n_consumed, gdn_stream_t stream);
+
 /* Checkpoint: bitwise copy of src's S and conv state into slot (device to
  * device), and of its committed length and tag. The slot is marked missing
  * (committed = -1) first and only filled in when the copy was launched, so a

@@ -1,0 +1,74 @@
+"""The no-allocation prefill (gdn_prefill_chunks_noalloc) against the regular one.
+
+This call serves callers that cannot allocate device memory: code whose memory
+a host framework plans once up front, and latency-critical code that must not
+call cudaMalloc / cudaFree (they can synchronise the device). Its scratch is a
+fixed array inside the library. These checks call it through the C ABI twice
+in a row on one session (the second call reuses the scratch the first one
+left behind) and compare each call's outputs and the session state with
+gdn_prefill_chunks on a twin session, within the parity tolerance. A call that
+needs more than the built-in scratch is refused before any device work.
+
+This file is collected last so that a stop at the first failure has already
+run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_deltanet_gb300 import gdn
+from chunked_gated_deltanet_gb300 import workloads as wl
+from helpers import TOL, Runner, out_rel, rel_l2_max
+
+pytestmark = pytest.mark.gpu
+
+
+def test_noalloc_matches_workspace_prefill_twice(cuda_device):
+    shape = wl.Shape(2, 4, 128, 128, 64, wl.BF16)
+    T1, T2 = 1000, 700           # first call on grid (consumes 960), second partial
+    w = wl.Workload("noalloc", shape, seed=31, session_lengths=[T1 + T2])
+    tok, cw = w.session_tokens(0), w.conv_weights()
+    run = Runner(shape, tok, cw, cuda_device)
+    a, b = run.session(), run.session()
+    oa, ob = run.new_out(), run.new_out()
+    tol_o, tol_s = TOL[wl.BF16]
+
+    def noalloc(sess, lo, hi, out, flags):
+        xq, xk, xv, g, beta = (x[lo:hi] for x in run.x)
+        return gdn.gdn_prefill_chunks_noalloc(run.desc, sess, xq, xk, xv, g, beta, run.cw_t, out[lo:hi],
+                                              flags=flags)
+
+    # call 1: on grid
+    n1 = noalloc(a, 0, T1, oa, 0)
+    m1 = run.prefill(b, 0, T1, ob, 0)
+    assert n1 == m1 == 960 and a.committed == b.committed == 960
+    torch.cuda.synchronize()
+    assert out_rel(oa[:n1].double().cpu().numpy(), ob[:n1].double().cpu().numpy()) <= tol_o
+    assert rel_l2_max(a.S.double().cpu().numpy(), b.S.double().cpu().numpy()) <= tol_s
+    # call 2: pending tail + the rest, partial allowed
+    n2 = noalloc(a, 960, T1 + T2, oa, gdn.GDN_ALLOW_PARTIAL)
+    m2 = run.prefill(b, 960, T1 + T2, ob, gdn.GDN_ALLOW_PARTIAL)
+    assert n2 == m2 == T1 + T2 - 960 and a.committed == b.committed == T1 + T2
+    torch.cuda.synchronize()
+    o_a, o_b = oa.double().cpu().numpy(), ob.double().cpu().numpy()
+    assert np.isfinite(o_a).all()
+    assert out_rel(o_a, o_b) <= tol_o
+    assert rel_l2_max(a.S.double().cpu().numpy(), b.S.double().cpu().numpy()) <= tol_s
+    assert torch.equal(a.conv, b.conv)
+
+
+def test_noalloc_refuses_calls_beyond_its_scratch(cuda_device):
+    shape = wl.Shape(16, 16, 128, 128, 512, wl.BF16)
+    desc = gdn.make_desc(16, 16, 128, 128, 512)
+    need = gdn.gdn_workspace_size(desc, 1024, 1)
+    assert need > gdn.GDN_NOALLOC_SCRATCH_BYTES
+    sess = gdn.Session(desc, cuda_device)
+    x = torch.zeros((1024, shape.channels), dtype=torch.bfloat16, device=cuda_device)
+    gb = torch.zeros((1024, 16), dtype=torch.float32, device=cuda_device)
+    out = torch.zeros((1024, 16, 128), dtype=torch.float32, device=cuda_device)
+    cw = torch.zeros((shape.channels, 4), dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.gdn_prefill_chunks_noalloc(desc, sess, x, x, x, gb, gb, cw, out)
+    assert e.value.status == gdn.GDN_ERR_WORKSPACE
+    assert "built-in" in str(e.value)
+    assert sess.committed == 0
