@@ -96,6 +96,12 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 WsLayout ws_layout(const gdn_layer_desc *d, int64_t nblk) {
     WsLayout L;
     const int D = d->d_k;
+    if (d->in_dtype == GDN_BF16) {  // tensor-core path: one record per (block, v-head)
+        L.qk_off = 0;
+        L.wu_off = 0;
+        L.bytes = align256((size_t)nblk * d->n_v_heads * gdn::rec_floats(D) * sizeof(float));
+        return L;
+    }
     L.qk_off = 0;
     L.wu_off = align256((size_t)nblk * d->n_qk_heads * gdn::qk_floats(D) * sizeof(float));
     L.bytes = L.wu_off + align256((size_t)nblk * d->n_v_heads * gdn::wu_floats(D) * sizeof(float));
@@ -316,11 +322,16 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
             i0 = i;
             if (cnt == 0) continue;
             p.n_sess = cnt; p.nblk = blk;
-            cudaError_t e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep(p, D, in_bf16, ch, cst); });
+            // bf16 inputs: tf32 tensor-core kernels; fp32 inputs: fp32 kernels (tighter tolerance)
+            cudaError_t e = launch_k(K_PREP, cst, [&] {
+                return in_bf16 ? gdn_launch_prep_tc(p, D, ch, cst) : gdn_launch_prep(p, D, in_bf16, ch, cst);
+            });
             if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
             e = launch_k(K_CONV, cst, [&] { return gdn_launch_conv_commit(p, D, in_bf16, ch, cst); });
             if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
-            e = launch_k(K_STATE, cst, [&] { return gdn_launch_state(p, D, cst); });
+            e = launch_k(K_STATE, cst, [&] {
+                return in_bf16 ? gdn_launch_chain_tc(p, D, cst) : gdn_launch_state(p, D, cst);
+            });
             if (e != cudaSuccess) return cuda_fail(e, "state/output kernel");
         }
     }

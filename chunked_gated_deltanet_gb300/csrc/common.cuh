@@ -38,6 +38,9 @@ struct LaunchCommon {
 // Per-(block, v-head) record in the workspace: W [64][D], U [64][D], P [64][64], gamma [64].
 __host__ __device__ constexpr int64_t wu_floats(int D) { return 2LL * kBlock * D + kBlock * kBlock + kBlock; }
 __host__ __device__ constexpr int64_t qk_floats(int D) { return 2LL * kBlock * D; }
+// Tensor-core path, per-(block, v-head) record: [W; Qe] [128][D] and K_tilde [64][D]
+// (tf32-rounded), U [64][D] and O_intra [64][D] (fp32), then e^{gamma_63} and padding.
+__host__ __device__ constexpr int64_t rec_floats(int D) { return 320LL * D + 16; }
 
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
@@ -69,6 +72,8 @@ void gdn_internal_set_error(const char *msg);
 // Launchers (host). Each returns cudaGetLastError() after its launch.
 cudaError_t gdn_launch_prep(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_state(const gdn::LaunchCommon &p, int D, cudaStream_t st);
+cudaError_t gdn_launch_prep_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
+cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, cudaStream_t st);
 cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *dst1, const void *src1,
                             size_t bytes1, cudaStream_t st);

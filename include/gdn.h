@@ -156,7 +156,7 @@ gdn_status gdn_prefill_varlen(const gdn_layer_desc *desc, gdn_session *sessions,
  * GDN_NOALLOC_SCRATCH_BYTES array inside the library, and the call allocates
  * nothing. A call whose processed tokens need more than that
  * (gdn_workspace_size(desc, tokens processed, 1) > GDN_NOALLOC_SCRATCH_BYTES;
- * about 830 tokens for 16 heads of d = 128) is refused with GDN_ERR_WORKSPACE
+ * about 700 tokens for 16 heads of d = 128) is refused with GDN_ERR_WORKSPACE
  * before any device work. The first call on a device looks up the scratch's
  * device address (cudaGetSymbolAddress) with that device current: make that
  * first call before any stream capture. All calls in the process share the

@@ -151,10 +151,12 @@ def test_decode_close_to_one_token_partial_prefill(cuda_device):
     gdn.gdn_decode_step(run.desc, [a], *(x[128:129] for x in run.x), run.cw_t, oa[128:129])
     run.prefill(b, 128, 129, ob, gdn.GDN_ALLOW_PARTIAL)
     torch.cuda.synchronize()
+    # the decode step is fp32; the bf16-input prefill runs on tf32 tensor cores: layer tolerance
+    tol_o, tol_s = TOL[wl.BF16]
     ra = oa[128].double().cpu().numpy()
     rb = ob[128].double().cpu().numpy()
-    assert np.linalg.norm(ra - rb) <= 1e-5 * np.linalg.norm(rb)
-    assert rel_l2_max(a.S.double().cpu().numpy(), b.S.double().cpu().numpy()) <= 1e-5
+    assert np.linalg.norm(ra - rb) <= tol_o * np.linalg.norm(rb)
+    assert rel_l2_max(a.S.double().cpu().numpy(), b.S.double().cpu().numpy()) <= tol_s
     assert torch.equal(a.conv, b.conv) and a.committed == b.committed == 129
 
 
