@@ -322,16 +322,20 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
             i0 = i;
             if (cnt == 0) continue;
             p.n_sess = cnt; p.nblk = blk;
-            // bf16 inputs: tf32 tensor-core kernels; fp32 inputs: fp32 kernels (tighter tolerance)
-            cudaError_t e = launch_k(K_PREP, cst, [&] {
-                return in_bf16 ? gdn_launch_prep_tc(p, D, ch, cst) : gdn_launch_prep(p, D, in_bf16, ch, cst);
-            });
-            if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
-            e = launch_k(K_CONV, cst, [&] { return gdn_launch_conv_commit(p, D, in_bf16, ch, cst); });
-            if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
-            e = launch_k(K_STATE, cst, [&] {
-                return in_bf16 ? gdn_launch_chain_tc(p, D, cst) : gdn_launch_state(p, D, cst);
-            });
+            cudaError_t e;
+            if (in_bf16) {
+                // bf16 inputs: tf32 tensor-core kernels; the state kernel also commits the conv state
+                e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep_tc(p, D, ch, cst); });
+                if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
+                e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_tc(p, D, ch, cst); });
+            } else {
+                // fp32 inputs: fp32 kernels (tighter tolerance)
+                e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep(p, D, in_bf16, ch, cst); });
+                if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
+                e = launch_k(K_CONV, cst, [&] { return gdn_launch_conv_commit(p, D, in_bf16, ch, cst); });
+                if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
+                e = launch_k(K_STATE, cst, [&] { return gdn_launch_state(p, D, cst); });
+            }
             if (e != cudaSuccess) return cuda_fail(e, "state/output kernel");
         }
     }

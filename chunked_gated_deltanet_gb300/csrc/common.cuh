@@ -38,9 +38,29 @@ struct LaunchCommon {
 // Per-(block, v-head) record in the workspace: W [64][D], U [64][D], P [64][64], gamma [64].
 __host__ __device__ constexpr int64_t wu_floats(int D) { return 2LL * kBlock * D + kBlock * kBlock + kBlock; }
 __host__ __device__ constexpr int64_t qk_floats(int D) { return 2LL * kBlock * D; }
-// Tensor-core path, per-(block, v-head) record: [W; Qe] [128][D] and K_tilde [64][D]
-// (tf32-rounded), U [64][D] and O_intra [64][D] (fp32), then e^{gamma_63} and padding.
+// Tensor-core path, per-(block, v-head) record (floats), laid out in the order
+// the state kernel's m16n8k8 fragments read it (g = lane / 4, t = lane % 4):
+//   [0, 128 D)      A fragments of [W; Qe] (128 x D): [m-tile 0..7][k-step 0..D/8-1][lane][4]
+//   [128 D, 192 D)  A fragments of K_tilde^T (D x 64): [m-tile 0..D/16-1][k-step 0..7][lane][4]
+//   [192 D, 256 D)  C fragments of U (64 x D) by 16-column slice: [slice][m-tile 0..3][n-tile 0..1][lane][4]
+//   [256 D, 320 D)  C fragments of O_intra, same order
+//   [320 D]         e^{gamma_63}, then padding to 320 D + 16
+// [W; Qe] and K_tilde are stored rounded to tf32; U and O_intra are fp32.
 __host__ __device__ constexpr int64_t rec_floats(int D) { return 320LL * D + 16; }
+constexpr int kSliceCols = 16;  // d_v columns per state-kernel CTA
+
+// Index of element (r, k) of an A operand with K columns inside its fragment-ordered array.
+__device__ __forceinline__ int afrag_index(int r, int k, int K) {
+    const int rr = r & 15, kk = k & 7;
+    const int lane = 4 * (rr & 7) + (kk & 3), f = (rr >> 3) + 2 * (kk >> 2);
+    return (((r >> 4) * (K >> 3) + (k >> 3)) * 32 + lane) * 4 + f;
+}
+// Index of element (i, c) of a 64 x D accumulator stored by 16-column slices of C fragments.
+__device__ __forceinline__ int cfrag_slice_index(int i, int c) {
+    const int sl = c >> 4, cc = c & 15, ri = i & 15;
+    const int lane = 4 * (ri & 7) + ((cc & 7) >> 1), f = 2 * (ri >> 3) + (cc & 1);
+    return ((((sl * 4 + (i >> 4)) * 2 + (cc >> 3)) * 32 + lane) * 4 + f);
+}
 
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
@@ -73,7 +93,7 @@ void gdn_internal_set_error(const char *msg);
 cudaError_t gdn_launch_prep(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_state(const gdn::LaunchCommon &p, int D, cudaStream_t st);
 cudaError_t gdn_launch_prep_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
-cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, cudaStream_t st);
+cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *dst1, const void *src1,
                             size_t bytes1, cudaStream_t st);

@@ -4,16 +4,16 @@
 // Per block (rows i = 0..63; rows >= n are padding and zero everywhere):
 //   conv (kernel 4, halo from the conv state at a call's first block), L2 norm
 //   gamma = cumulative log-decay in the block
-//   QK^T, KK^T                                     split-tf32 MMA (lower triangle only)
+//   Q K^T, K K^T                                    split-tf32 MMA, lower triangle
 //   A_ij = beta_i e^{gamma_i - gamma_j} (K K^T)_ij      (j < i)
-//   P_ij = e^{gamma_i - gamma_j} (Q K^T)_ij             (j <= i)
-//   (I + A) [W | U] = [diag(beta e^gamma) K_hat | diag(beta) V]   forward substitution
-//   Qe = diag(e^gamma) Q_hat - P W,  O_intra = P U       tf32 MMA
+//   T = (I + A)^{-1}                                 blocked 16 x 16 inverse, fp32
+//   W = T diag(beta e^gamma) K_hat,  U = T diag(beta) V     split-tf32 MMA
+//   P_ij = e^{gamma_i - gamma_j} (Q K^T)_ij              (j <= i)
+//   Qe = diag(e^gamma) Q_hat - P W,  O_intra = P U          tf32 MMA
 //   K_tilde = diag(e^{gamma_63 - gamma_j}) K_hat
 // so that, with S0 the state entering the block, the outputs are
 // O = Qe S0^T + O_intra and U' = U - W S0^T feeds S^T <- e^{gamma_63} S0^T + K_tilde^T U'.
-// Record per (block, v-head), in floats: [W; Qe] [128][D] and K_tilde [64][D]
-// (both pre-rounded to tf32), U [64][D], O_intra [64][D], e^{gamma_63}.
+// The record is written in the fragment order of the state kernel (see common.cuh).
 #include "common.cuh"
 #include "mma.cuh"
 
@@ -22,27 +22,28 @@ namespace gdn {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon p, int64_t ch) {
     extern __shared__ __align__(16) float smem[];
-    constexpr int LQ = D + 4;       // q_hat / k_hat rows: A-fragment reads hit 32 distinct banks
-    constexpr int LA = kBlock + 1;  // 64 x 64 tiles written from fragments / read as scalars
-    constexpr int LX = 2 * D + 8;   // [W | U]: B-fragment reads hit 32 distinct banks
-    constexpr int LP = kBlock + 4;  // P: A-fragment reads
-    constexpr int RAW = (kBlock + 3) * D;  // raw bf16 tile, halo rows first
+    constexpr int LQ = D + 4;       // q_hat / k_hat rows: row-indexed A fragments, banks 4g + t
+    constexpr int LA = kBlock + 1;  // Q K^T, K K^T
+    constexpr int LT = kBlock + 4;  // T, A and P: row-indexed A fragments
+    constexpr int LB = D + 8;       // B operands indexed [token][column]: banks 8t + g
+    constexpr int RAW = (kBlock + 3) * D;
     float *Yq = smem;
     float *Yk = Yq + kBlock * LQ;
     float *QK = Yk + kBlock * LQ;
     float *KK = QK + kBlock * LA;
-    float *Am = KK + kBlock * LA;
-    float *X = Am + kBlock * LA;
-    float *Ps = X + kBlock * LX;
-    float *gam = Ps + kBlock * LP;
+    float *Tm = KK + kBlock * LA;
+    float *Ps = Tm + kBlock * LT;   // A during the inverse, then P
+    float *Bk = Ps + kBlock * LT;   // raw q/k, raw v, inverse scratch, then beta e^gamma k_hat, then W
+    float *Bv = Bk + kBlock * LB;   // beta v, then U
+    float *gam = Bv + kBlock * LB;
     float *bet = gam + kBlock;
-    float *eg = bet + kBlock;
-    // raw input tiles alias regions that are free at the time
-    __nv_bfloat16 *rawq = reinterpret_cast<__nv_bfloat16 *>(X);
+    float *egv = bet + kBlock;
+    __nv_bfloat16 *rawq = reinterpret_cast<__nv_bfloat16 *>(Bk);
     __nv_bfloat16 *rawk = rawq + RAW;
-    __nv_bfloat16 *rawv = reinterpret_cast<__nv_bfloat16 *>(Ps);
-    static_assert(2 * RAW * 2 <= kBlock * LX * 4, "q/k raw tiles must fit the X region");
-    static_assert(RAW * 2 <= kBlock * LP * 4, "v raw tile must fit the P region");
+    __nv_bfloat16 *rawv = reinterpret_cast<__nv_bfloat16 *>(Bk);
+    float *Mt = Bk + (RAW + 1) / 2 + 4;   // inverse scratch, after the raw v tile
+    static_assert(2 * RAW * 2 <= kBlock * LB * 4, "q/k raw tiles must fit the Bk region");
+    static_assert((RAW + 1) / 2 + 4 + 3 * 16 * 17 <= kBlock * LB, "inverse scratch must fit the Bk region");
 
     const int blk = blockIdx.x, hk = blockIdx.y, t = threadIdx.x;
     const int warp = t >> 5, lane = t & 31, g8 = lane >> 2, t4 = lane & 3;
@@ -55,11 +56,10 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
     const __nv_bfloat16 *cw = static_cast<const __nv_bfloat16 *>(p.conv_w);
     const __nv_bfloat16 *cs = static_cast<const __nv_bfloat16 *>(s.conv);
 
-    // Stage rows pos0-3 .. pos0+63 of one head's channels into shared memory.
-    // Rows before the call come from the conv state; rows past the block's valid
-    // rows are zero-filled.
+    // Stage rows pos0-3 .. pos0+63 of one head's channels; rows before the call
+    // come from the conv state, rows past the block's valid rows are zero.
     auto stage = [&](__nv_bfloat16 *dst, const __nv_bfloat16 *x, int64_t ld, int64_t col0, int64_t chan0) {
-        constexpr int CH = D / 8;  // 16-byte chunks per row
+        constexpr int CH = D / 8;
         for (int e = t; e < (kBlock + 3) * CH; e += kThreads) {
             const int r = e / CH, c = (e % CH) * 8;
             const int pos = pos0 - 3 + r;
@@ -72,13 +72,11 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
         }
         cp_async_commit();
     };
-    // Conv of channel c of a staged tile into out[i * ldo + c] * scale_i (scale 1 if null).
     auto conv_ch = [&](const __nv_bfloat16 *raw, int c, int64_t chan, float *out, int ldo, const float *rowscale) {
         float w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) w[i] = __bfloat162float(cw[chan * 4 + i]);
-        float h3 = __bfloat162float(raw[0 * D + c]), h2 = __bfloat162float(raw[1 * D + c]);
-        float h1 = __bfloat162float(raw[2 * D + c]);
+        float h3 = __bfloat162float(raw[c]), h2 = __bfloat162float(raw[D + c]), h1 = __bfloat162float(raw[2 * D + c]);
 #pragma unroll 8
         for (int i = 0; i < kBlock; ++i) {
             const float x0 = __bfloat162float(raw[(i + 3) * D + c]);
@@ -88,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
         }
     };
 
-    // 1. q and k tiles -> conv
+    // 1. q and k: stage, conv, L2 norm
     stage(rawq, static_cast<const __nv_bfloat16 *>(p.xq), nq, (int64_t)hk * D, (int64_t)hk * D);
     stage(rawk, static_cast<const __nv_bfloat16 *>(p.xk), nq, (int64_t)hk * D, nq + (int64_t)hk * D);
     cp_async_wait<0>();
@@ -98,8 +96,6 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
         conv_ch(which ? rawk : rawq, c, which * nq + (int64_t)hk * D + c, which ? Yk : Yq, LQ, nullptr);
     }
     __syncthreads();
-
-    // 2. L2 norm per row; padding rows zero
     for (int r = warp; r < 2 * kBlock; r += kThreads / 32) {
         const int i = r % kBlock;
         float *row = (r < kBlock ? Yq : Yk) + i * LQ;
@@ -112,7 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
     }
     __syncthreads();
 
-    // 3. QK^T and KK^T on the 20 lower-triangle 16x8 tiles (m-tile mi, n-tile nj <= 2 mi + 1)
+    // 2. Q K^T and K K^T on the 20 lower-triangle 16x8 tiles, split tf32 (these
+    //    dot products of unit vectors can cancel; one rounding would show in short sequences)
     for (int tile = warp; tile < 20; tile += kThreads / 32) {
         int mi = 0, rem = tile;
         while (rem >= 2 * mi + 2) { rem -= 2 * mi + 2; ++mi; }
@@ -121,8 +118,6 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
         const float *qa = Yq + (16 * mi + g8) * LQ + t4;
         const float *ka = Yk + (16 * mi + g8) * LQ + t4;
         const float *kb = Yk + (8 * nj + g8) * LQ + t4;
-        // split tf32 (hi*hi + hi*lo + lo*hi): these dot products of unit vectors can cancel,
-        // and a single rounding of the operands would show in short sequences
 #pragma unroll 2
         for (int k0 = 0; k0 < D; k0 += 8) {
             uint32_t aqh[4], aql[4], akh[4], akl[4], bh[2], bl[2];
@@ -150,13 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
         KK[(i0 + 8) * LA + j0] = ck[2]; KK[(i0 + 8) * LA + j0 + 1] = ck[3];
     }
 
-    // 4. each v-head of the group
+    // 3. each v-head of the group
     for (int gi = 0; gi < p.G; ++gi) {
         const int h = hk * p.G + gi;
-        __syncthreads();  // QK/KK written; the previous head's X and P consumed
+        __syncthreads();  // QK/KK written; the previous head's buffers consumed
         stage(rawv, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)h * D, 2 * nq + (int64_t)h * D);
-        // gamma: inclusive scan of g over the block (two warps), beta
-        if (t < kBlock) {
+        if (t < kBlock) {   // gamma: inclusive scan of g (two warps), beta
             float gv = t < n ? p.g[(row0 + t) * Hv + h] : 0.f;
             const float bv = t < n ? p.beta[(row0 + t) * Hv + h] : 0.f;
 #pragma unroll
@@ -171,43 +165,119 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
         if (t >= 32 && t < kBlock) gam[t] += gam[31];
         cp_async_wait<0>();
         __syncthreads();
-        if (t < kBlock) eg[t] = expf(gam[t]);
-        // A (strict lower), rhs of W, v conv -> rhs of U
-        for (int e = t; e < kBlock * kBlock; e += kThreads) {
+        if (t < kBlock) egv[t] = expf(gam[t]);
+        for (int e = t; e < kBlock * kBlock; e += kThreads) {   // A (strict lower) into the P buffer
             const int i = e / kBlock, j = e % kBlock;
-            Am[i * LA + j] = j < i ? bet[i] * expf(gam[i] - gam[j]) * KK[i * LA + j] : 0.f;
+            Ps[i * LT + j] = j < i ? bet[i] * expf(gam[i] - gam[j]) * KK[i * LA + j] : 0.f;
         }
-        if (t < D) {
-            conv_ch(rawv, t, 2 * nq + (int64_t)h * D + t, X + D, LX, bet);
-        } else if (t < 2 * D) {
-            const int c = t - D;
-            for (int i = 0; i < kBlock; ++i) X[i * LX + c] = (bet[i] * expf(gam[i])) * Yk[i * LQ + c];
+        if (t < D) conv_ch(rawv, t, 2 * nq + (int64_t)h * D + t, Bv, LB, bet);   // beta v
+        __syncthreads();
+
+        // T = (I + A)^{-1}: diagonal 16x16 blocks by substitution, one column per thread
+        if (t < kBlock) {
+            const int d = t >> 4, c = t & 15;
+            const float *Ad = Ps + 16 * d * LT + 16 * d;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float sum = 0.f;
+#pragma unroll
+                for (int j = 0; j < i; ++j)
+                    if (j >= c) sum = fmaf(Ad[i * LT + j], x[j], sum);
+                x[i] = i < c ? 0.f : (i == c ? 1.f : -sum);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tm[(16 * d + i) * LT + 16 * d + c] = x[i];
         }
         __syncthreads();
-        // P (overwrites the raw v tile) and the forward substitution (I + A) X = rhs
+        // off-diagonal blocks by distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+        for (int dist = 1; dist < 4; ++dist) {
+            const int nblkd = 4 - dist;
+            for (int e = t; e < nblkd * 256; e += kThreads) {
+                const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15, ib = jb + dist;
+                float sum = 0.f;
+                for (int k = 16 * jb; k < 16 * ib; ++k) sum = fmaf(Ps[(16 * ib + r) * LT + k], Tm[k * LT + 16 * jb + c], sum);
+                Mt[(jb * 16 + r) * 17 + c] = sum;
+            }
+            __syncthreads();
+            for (int e = t; e < nblkd * 256; e += kThreads) {
+                const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15, ib = jb + dist;
+                float sum = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) sum = fmaf(Tm[(16 * ib + r) * LT + 16 * ib + k], Mt[(jb * 16 + k) * 17 + c], sum);
+                Tm[(16 * ib + r) * LT + 16 * jb + c] = -sum;
+            }
+            __syncthreads();
+        }
+        // B operands: beta e^gamma k_hat (over the raw tile and scratch); P over A
+        for (int e = t; e < kBlock * D; e += kThreads) {
+            const int i = e / D, c = e % D;
+            Bk[i * LB + c] = (bet[i] * egv[i]) * Yk[i * LQ + c];
+        }
         for (int e = t; e < kBlock * kBlock; e += kThreads) {
             const int i = e / kBlock, j = e % kBlock;
-            Ps[i * LP + j] = j <= i ? QK[i * LA + j] * expf(gam[i] - gam[j]) : 0.f;
-        }
-        if (t < 2 * D) {
-            const int c = t;
-            for (int i = 1; i < kBlock; ++i) {
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                int j = 0;
-                for (; j + 4 <= i; j += 4) {
-                    a0 = fmaf(Am[i * LA + j], X[j * LX + c], a0);
-                    a1 = fmaf(Am[i * LA + j + 1], X[(j + 1) * LX + c], a1);
-                    a2 = fmaf(Am[i * LA + j + 2], X[(j + 2) * LX + c], a2);
-                    a3 = fmaf(Am[i * LA + j + 3], X[(j + 3) * LX + c], a3);
-                }
-                for (; j < i; ++j) a0 = fmaf(Am[i * LA + j], X[j * LX + c], a0);
-                X[i * LX + c] -= (a0 + a1) + (a2 + a3);
-            }
+            Ps[i * LT + j] = j <= i ? QK[i * LA + j] * expf(gam[i] - gam[j]) : 0.f;
         }
         __syncthreads();
 
         float *rec = p.ws_wu + ((int64_t)blk * Hv + h) * rec_floats(D);
-        // Qe = e^gamma Q_hat - P W and O_intra = P U: warp w owns n-tiles [w*NT, w*NT + NT) of both
+        // W = T Bk (warps 0-3) and U = T Bv (warps 4-7), split tf32, T lower triangular
+        {
+            constexpr int NW = D / 32;   // n-tiles per warp
+            const float *B = warp < 4 ? Bk : Bv;
+            const int nbase = (warp & 3) * NW * 8;
+            float acc[4][NW][4];
+#pragma unroll
+            for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+                for (int nt = 0; nt < NW; ++nt)
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) acc[mi][nt][f] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t bh[NW][2], bl[NW][2];
+#pragma unroll
+                for (int nt = 0; nt < NW; ++nt) {
+                    const int n0 = nbase + nt * 8 + g8;
+                    split_tf32(B[(8 * kk + t4) * LB + n0], bh[nt][0], bl[nt][0]);
+                    split_tf32(B[(8 * kk + t4 + 4) * LB + n0], bh[nt][1], bl[nt][1]);
+                }
+#pragma unroll
+                for (int mi = 0; mi < 4; ++mi) {
+                    if (mi < kk / 2) continue;
+                    const float *ta = Tm + (16 * mi + g8) * LT + 8 * kk + t4;
+                    uint32_t ah[4], al[4];
+                    split_tf32(ta[0], ah[0], al[0]);
+                    split_tf32(ta[8 * LT], ah[1], al[1]);
+                    split_tf32(ta[4], ah[2], al[2]);
+                    split_tf32(ta[8 * LT + 4], ah[3], al[3]);
+#pragma unroll
+                    for (int nt = 0; nt < NW; ++nt) {
+                        mma_tf32(acc[mi][nt], al, bh[nt]);
+                        mma_tf32(acc[mi][nt], ah, bl[nt]);
+                        mma_tf32(acc[mi][nt], ah, bh[nt]);
+                    }
+                }
+            }
+            __syncthreads();   // every warp is done reading Bk / Bv
+            float *dst = warp < 4 ? Bk : Bv;
+#pragma unroll
+            for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+                for (int nt = 0; nt < NW; ++nt) {
+                    const int c = nbase + nt * 8 + 2 * t4, i = 16 * mi + g8;
+                    dst[i * LB + c] = acc[mi][nt][0];
+                    dst[i * LB + c + 1] = acc[mi][nt][1];
+                    dst[(i + 8) * LB + c] = acc[mi][nt][2];
+                    dst[(i + 8) * LB + c + 1] = acc[mi][nt][3];
+                    if (warp >= 4)   // U goes out as-is, in C-fragment slice order
+                        *reinterpret_cast<float4 *>(rec + 192 * D + cfrag_slice_index(i, c)) =
+                            make_float4(acc[mi][nt][0], acc[mi][nt][1], acc[mi][nt][2], acc[mi][nt][3]);
+                }
+        }
+        __syncthreads();
+
+        // Qe = e^gamma Q_hat - P W and O_intra = P U (tf32): warp w owns n-tiles [w*NT, w*NT + NT) of both
         {
             constexpr int NT = D / 64;
             float aq[4][NT][4], ao[4][NT][4];
@@ -223,17 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int n0 = (warp * NT + nt) * 8 + g8;
-                    bw[nt][0] = tf32_bits(X[(8 * kk + t4) * LX + n0]);
-                    bw[nt][1] = tf32_bits(X[(8 * kk + t4 + 4) * LX + n0]);
-                    bu[nt][0] = tf32_bits(X[(8 * kk + t4) * LX + D + n0]);
-                    bu[nt][1] = tf32_bits(X[(8 * kk + t4 + 4) * LX + D + n0]);
+                    bw[nt][0] = tf32_bits(Bk[(8 * kk + t4) * LB + n0]);
+                    bw[nt][1] = tf32_bits(Bk[(8 * kk + t4 + 4) * LB + n0]);
+                    bu[nt][0] = tf32_bits(Bv[(8 * kk + t4) * LB + n0]);
+                    bu[nt][1] = tf32_bits(Bv[(8 * kk + t4 + 4) * LB + n0]);
                 }
 #pragma unroll
                 for (int mi = 0; mi < 4; ++mi) {
                     if (mi < kk / 2) continue;  // P is lower triangular
-                    const float *pa = Ps + (16 * mi + g8) * LP + 8 * kk + t4;
-                    const uint32_t a[4] = {tf32_bits(pa[0]), tf32_bits(pa[8 * LP]), tf32_bits(pa[4]),
-                                           tf32_bits(pa[8 * LP + 4])};
+                    const float *pa = Ps + (16 * mi + g8) * LT + 8 * kk + t4;
+                    const uint32_t a[4] = {tf32_bits(pa[0]), tf32_bits(pa[8 * LT]), tf32_bits(pa[4]),
+                                           tf32_bits(pa[8 * LT + 4])};
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         mma_tf32(aq[mi][nt], a, bw[nt]);
@@ -241,52 +311,55 @@ __global__ void __launch_bounds__(kThreads, 1) prep_tc_kernel(const LaunchCommon
                     }
                 }
             }
-            float *Qe = rec + kBlock * D, *Oi = rec + 4 * kBlock * D;
 #pragma unroll
             for (int mi = 0; mi < 4; ++mi)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const int c = (warp * NT + nt) * 8 + 2 * t4;
+                    const int c = (warp * NT + nt) * 8 + 2 * t4, i = 16 * mi + g8;
+                    *reinterpret_cast<float4 *>(rec + 256 * D + cfrag_slice_index(i, c)) =
+                        make_float4(ao[mi][nt][0], ao[mi][nt][1], ao[mi][nt][2], ao[mi][nt][3]);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int i = 16 * mi + g8 + 8 * hh;
-                        const float e = eg[i];
-                        float2 q2, o2;
-                        q2.x = tf32_round(e * Yq[i * LQ + c] - aq[mi][nt][2 * hh]);
-                        q2.y = tf32_round(e * Yq[i * LQ + c + 1] - aq[mi][nt][2 * hh + 1]);
-                        o2.x = ao[mi][nt][2 * hh];
-                        o2.y = ao[mi][nt][2 * hh + 1];
-                        *reinterpret_cast<float2 *>(&Qe[i * D + c]) = q2;
-                        *reinterpret_cast<float2 *>(&Oi[i * D + c]) = o2;
+                    for (int f = 0; f < 4; ++f) {
+                        const int ii = i + 8 * (f >> 1), cc = c + (f & 1);
+                        rec[afrag_index(kBlock + ii, cc, D)] = tf32_round(egv[ii] * Yq[ii * LQ + cc] - aq[mi][nt][f]);
                     }
                 }
         }
-        // W (tf32), K_tilde (tf32), U (fp32), e^{gamma_63}
+        // W (rows 0..63 of [W; Qe]) and K_tilde^T as A fragments, tf32; e^{gamma_63}
         {
             const float gl = gam[kBlock - 1];
-            float *W = rec, *Kt = rec + 2 * kBlock * D, *U = rec + 3 * kBlock * D;
-            for (int e = t; e < kBlock * D / 4; e += kThreads) {
-                const int i = e / (D / 4), c = (e % (D / 4)) * 4;
-                const float4 xw = *reinterpret_cast<const float4 *>(&X[i * LX + c]);
-                const float4 xu = *reinterpret_cast<const float4 *>(&X[i * LX + D + c]);
-                const float4 kk = *reinterpret_cast<const float4 *>(&Yk[i * LQ + c]);
-                const float dj = expf(gl - gam[i]);
-                *reinterpret_cast<float4 *>(&W[i * D + c]) =
-                    make_float4(tf32_round(xw.x), tf32_round(xw.y), tf32_round(xw.z), tf32_round(xw.w));
-                *reinterpret_cast<float4 *>(&Kt[i * D + c]) = make_float4(
-                    tf32_round(dj * kk.x), tf32_round(dj * kk.y), tf32_round(dj * kk.z), tf32_round(dj * kk.w));
-                *reinterpret_cast<float4 *>(&U[i * D + c]) = xu;
+            constexpr int NW4 = 4 * (D / 8) * 32;   // float4 groups of W
+            for (int e = t; e < NW4 + (D / 16) * 8 * 32; e += kThreads) {
+                const bool isw = e < NW4;
+                const int q = isw ? e : e - NW4, ln = q & 31, tile = q >> 5;
+                const int gg = ln >> 2, tt = ln & 3;
+                float v[4];
+                if (isw) {
+                    const int mt = tile / (D / 8), ks = tile % (D / 8);
+#pragma unroll
+                    for (int f = 0; f < 4; ++f)
+                        v[f] = tf32_round(Bk[(16 * mt + gg + 8 * (f & 1)) * LB + 8 * ks + tt + 4 * (f >> 1)]);
+                    *reinterpret_cast<float4 *>(rec + q * 4) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+                    const int mt = tile >> 3, ks = tile & 7;
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const int m = 16 * mt + gg + 8 * (f & 1), k = 8 * ks + tt + 4 * (f >> 1);
+                        v[f] = tf32_round(expf(gl - gam[k]) * Yk[k * LQ + m]);
+                    }
+                    *reinterpret_cast<float4 *>(rec + 128 * D + q * 4) = make_float4(v[0], v[1], v[2], v[3]);
+                }
             }
-            if (t == 0) rec[5 * kBlock * D] = expf(gl);
+            if (t == 0) rec[320 * D] = expf(gl);
         }
     }
 }
 
 template <int D>
 static cudaError_t launch(const LaunchCommon &p, int64_t ch, cudaStream_t st) {
-    constexpr int LQ = D + 4, LA = kBlock + 1, LX = 2 * D + 8, LP = kBlock + 4;
+    constexpr int LQ = D + 4, LA = kBlock + 1, LT = kBlock + 4, LB = D + 8;
     constexpr size_t smem =
-        sizeof(float) * (2 * kBlock * LQ + 3 * kBlock * LA + kBlock * LX + kBlock * LP + 3 * kBlock);
+        sizeof(float) * (2 * kBlock * LQ + 2 * kBlock * LA + 2 * kBlock * LT + 2 * kBlock * LB + 3 * kBlock);
     auto k = prep_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
