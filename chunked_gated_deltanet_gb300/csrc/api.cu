@@ -108,9 +108,16 @@ WsLayout ws_layout(const gdn_layer_desc *d, int64_t nblk) {
     return L;
 }
 
+// Bounded waits: default poll limit, and the test hook that makes the next launches' waits run out.
+constexpr long long kDefaultWaitLimit = 1LL << 24;
+long long g_wait_limit = kDefaultWaitLimit;
+int g_skip_first_copy = 0;
+
 void fill_common(LaunchCommon &p, const gdn_layer_desc *d, const void *xq, const void *xk, const void *xv,
                  const float *g, const float *beta, const void *conv_w, void *out) {
     std::memset(&p, 0, sizeof(p));
+    p.wait_limit = g_wait_limit;
+    p.debug_skip_first_copy = g_skip_first_copy;
     p.xq = xq; p.xk = xk; p.xv = xv; p.g = g; p.beta = beta; p.conv_w = conv_w; p.out = out;
     p.Hk = d->n_qk_heads; p.Hv = d->n_v_heads; p.G = d->n_v_heads / d->n_qk_heads;
     p.act = d->conv_act; p.out_bf16 = d->out_dtype == GDN_BF16;
@@ -448,6 +455,26 @@ GDN_API gdn_status gdn_decode_step(const gdn_layer_desc *d, gdn_session *session
         if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
     }
     for (int i = 0; i < n; ++i) sessions[i].committed += 1;
+    return GDN_OK;
+}
+
+GDN_API gdn_status gdn_device_status(gdn_stream_t stream) {
+    unsigned int word = 0;
+    cudaError_t e = gdn_take_device_error(&word, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "device status read");
+    if (word & 1u) return fail(GDN_ERR_TIMEOUT, "a kernel gave up waiting for its operand copies");
+    return GDN_OK;
+}
+
+GDN_API gdn_status gdn_debug_inject_wait_timeout(int32_t enable, int64_t wait_limit) {
+    if (!enable) {
+        g_skip_first_copy = 0;
+        g_wait_limit = kDefaultWaitLimit;
+        return GDN_OK;
+    }
+    if (wait_limit < 1) return fail(GDN_ERR_INVALID_ARG, "wait_limit must be >= 1");
+    g_skip_first_copy = 1;
+    g_wait_limit = wait_limit;
     return GDN_OK;
 }
 

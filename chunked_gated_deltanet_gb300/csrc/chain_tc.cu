@@ -1,18 +1,23 @@
 // Sequential state pass and outputs on tensor cores (bf16-input path): one CTA
 // per (session, v-head, 16-column slice of d_v), 8 warps, walking the
-// session's 64-token blocks strictly in position order. Per block, with the
-// fp32 state slice S^T [D][16] in shared memory:
+// session's 64-token blocks strictly in position order. Per block:
 //   Z = [W; Qe] S^T                  (128 x 16; warp w owns rows 16w..16w+15)
 //   U' = U - Z[0:64],  O = Z[64:128] + O_intra   (outputs written here)
 //   S^T <- e^{gamma_63} S^T + K_tilde^T U'        (warp w owns state rows 16w..16w+15)
-// Operands are tf32 (pre-rounded by the prologue, or rounded here for S^T and
-// U'), accumulation is fp32, and the state itself stays fp32. The prologue
-// stores each block's operands in fragment order, so one block is one
-// contiguous copy; a two-stage cp.async pipeline fetches block b+1 while
-// block b is computed. The CTA also commits its share of the session's conv
-// state (nothing in this kernel reads it).
+// The fp32 state lives in the registers of the warps that own its rows (in
+// m16n8 accumulator layout); shared memory holds its tf32 copy, the B operand
+// of the next block's first product. Operands are tf32 (rounded by the
+// prologue, or here for U'), accumulation is fp32. The prologue stores each
+// block's operands in fragment order, so a block is five contiguous bulk
+// copies (TMA), issued by one thread into a two-stage buffer and completed on
+// an mbarrier; block b+1 loads while block b computes. Every wait on an
+// mbarrier is bounded: on timeout the CTA records GDN_ERR_TIMEOUT in the
+// device error word, waits (bounded) for its copies in flight, and returns.
+// The CTA also commits its share of the session's conv state.
 #include "common.cuh"
 #include "mma.cuh"
+
+__device__ unsigned int g_gdn_device_error;
 
 namespace gdn {
 
@@ -20,14 +25,15 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommon p, int64_t ch) {
     extern __shared__ __align__(16) float smem[];
     constexpr int DS = kSliceCols, NT = DS / 8;
-    constexpr int SP = DS + 8;                 // S^T and U' rows (B fragments): banks 24t + g, distinct
+    constexpr int SP = DS + 8;                 // tf32 S^T and U' rows (B fragments): banks 24t + g, distinct
     constexpr int WQF = 2 * kBlock * D;        // [W; Qe] fragments
     constexpr int KTF = kBlock * D;            // K_tilde^T fragments
     constexpr int UF = kBlock * DS;            // one slice of U (or O_intra) fragments
     constexpr int STAGE = WQF + KTF + 2 * UF + 4;
     static_assert(D == 128 || D == 64, "head dim");
-    float *St = smem + 2 * STAGE;              // [D][SP]   fp32 state slice
+    float *St = smem + 2 * STAGE;              // [D][SP]   tf32 copy of the state slice
     float *Ups = St + D * SP;                  // [64][SP]  tf32 U'
+    uint64_t *bar = reinterpret_cast<uint64_t *>(Ups + kBlock * SP);   // [2] stage barriers
 
     constexpr int nsl = D / DS;
     const int sl = blockIdx.x % nsl;
@@ -38,6 +44,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
     const int Hv = p.Hv;
     const int nb = (s.n + kBlock - 1) / kBlock;
     const int64_t RF = rec_floats(D);
+    const bool owner = 16 * warp < D;          // this warp owns state rows 16w..16w+15
+    const int m0 = 16 * warp + g8;
 
     // conv-state commit: the raw inputs at the session's last three processed positions
     {
@@ -63,28 +71,56 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
         }
     }
 
+    // block b's operands -> stage b & 1 (thread 0 only)
     auto issue = [&](int b) {
         float *buf = smem + (b & 1) * STAGE;
         const float *r = p.ws_wu + ((int64_t)(s.blk0 + b) * Hv + h) * RF;
-        for (int e = t; e < (WQF + KTF) / 4; e += kThreads) cp_async16(buf + 4 * e, r + 4 * e);
-        for (int e = t; e < 2 * UF / 4; e += kThreads) {
-            const int which = e / (UF / 4), q = e % (UF / 4);
-            cp_async16(buf + WQF + KTF + which * UF + 4 * q, r + (192 + 64 * which) * D + sl * UF + 4 * q);
-        }
-        if (t == 0) cp_async16(buf + WQF + KTF + 2 * UF, r + 320 * D);
+        uint64_t *br = &bar[b & 1];
+        if (b == 0 && p.debug_skip_first_copy) return;   // test hook: leave the barrier pending
+        fence_proxy_async();
+        mbar_arrive_expect_tx(br, (uint32_t)sizeof(float) * (WQF + KTF + 2 * UF + 4));
+        constexpr int CHUNK = 4096;   // floats per bulk copy (16 KB)
+        static_assert((WQF + KTF) % CHUNK == 0, "operand block is a whole number of chunks");
+#pragma unroll
+        for (int q = 0; q < (WQF + KTF) / CHUNK; ++q) bulk_g2s(buf + q * CHUNK, r + q * CHUNK, sizeof(float) * CHUNK, br);
+        bulk_g2s(buf + WQF + KTF, r + 192 * D + sl * UF, sizeof(float) * UF, br);
+        bulk_g2s(buf + WQF + KTF + UF, r + 256 * D + sl * UF, sizeof(float) * UF, br);
+        bulk_g2s(buf + WQF + KTF + 2 * UF, r + 320 * D, 16, br);
     };
 
+    // state rows in registers (fp32), tf32 copy in shared memory
     float *Sg = s.S + (int64_t)h * D * D;
-    for (int e = t; e < D * DS; e += kThreads) St[(e / DS) * SP + e % DS] = Sg[(int64_t)(e / DS) * D + c0 + e % DS];
-    if (nb > 0) issue(0);
-    cp_async_commit();
+    float st[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int c = 8 * nt + 2 * t4;
+        if (owner) {
+            st[nt][0] = Sg[(int64_t)m0 * D + c0 + c];
+            st[nt][1] = Sg[(int64_t)m0 * D + c0 + c + 1];
+            st[nt][2] = Sg[(int64_t)(m0 + 8) * D + c0 + c];
+            st[nt][3] = Sg[(int64_t)(m0 + 8) * D + c0 + c + 1];
+            St[m0 * SP + c] = tf32_round(st[nt][0]);
+            St[m0 * SP + c + 1] = tf32_round(st[nt][1]);
+            St[(m0 + 8) * SP + c] = tf32_round(st[nt][2]);
+            St[(m0 + 8) * SP + c + 1] = tf32_round(st[nt][3]);
+        } else {
+            st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.f;
+        }
+    }
+    if (t == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (t == 0 && nb > 0) issue(0);
 
+    int timed_out = 0;
     for (int b = 0; b < nb; ++b) {
         const float *buf = smem + (b & 1) * STAGE;
-        if (b + 1 < nb) issue(b + 1);   // the other stage was released at the end of step b-1
-        cp_async_commit();
-        cp_async_wait<1>();             // block b's group has landed (this thread's part)
-        __syncthreads();                // (A) ... and everyone's
+        if (t == 0 && b + 1 < nb) issue(b + 1);   // the other stage was released at the end of step b-1
+        const bool ok = mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
+        if (__syncthreads_or(!ok)) { timed_out = b + 1; break; }   // (A) uniform decision
 
         // Z = [W; Qe] S^T, two partial accumulators (even / odd k-steps) per n-tile
         float acc[NT][4], acc2[NT][4];
@@ -102,8 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
                 const int k0 = 8 * ks;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint32_t bb[2] = {tf32_bits(St[(k0 + t4) * SP + 8 * nt + g8]),
-                                            tf32_bits(St[(k0 + t4 + 4) * SP + 8 * nt + g8])};
+                    const uint32_t bb[2] = {__float_as_uint(St[(k0 + t4) * SP + 8 * nt + g8]),
+                                            __float_as_uint(St[(k0 + t4 + 4) * SP + 8 * nt + g8])};
                     mma_tf32((ks & 1) ? acc2[nt] : acc[nt], a, bb);
                 }
             }
@@ -140,22 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
                 }
             }
         }
-        __syncthreads();  // (B) U' complete
-        // S^T <- e^{gamma_63} S^T + K_tilde^T U'   (D / 16 warps own the state rows)
-        if (16 * warp < D) {
+        __syncthreads();  // (B) U' complete; every read of the tf32 state copy done
+        // S^T <- e^{gamma_63} S^T + K_tilde^T U' on the owner warps' registers
+        if (owner) {
             const float e = buf[WQF + KTF + 2 * UF];
-            const int m0 = 16 * warp + g8;
-            float cst[NT][4], cst2[NT][4];
+            float cst2[NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int c = 8 * nt + 2 * t4;
-                cst[nt][0] = e * St[m0 * SP + c];
-                cst[nt][1] = e * St[m0 * SP + c + 1];
-                cst[nt][2] = e * St[(m0 + 8) * SP + c];
-                cst[nt][3] = e * St[(m0 + 8) * SP + c + 1];
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int f = 0; f < 4; ++f) cst2[nt][f] = 0.f;
-            }
+                for (int f = 0; f < 4; ++f) {
+                    st[nt][f] *= e;
+                    cst2[nt][f] = 0.f;
+                }
             const float4 *ka = reinterpret_cast<const float4 *>(buf + WQF) + (warp * 8) * 32 + lane;
 #pragma unroll
             for (int ks = 0; ks < kBlock / 8; ++ks) {
@@ -167,30 +199,51 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint32_t bb[2] = {__float_as_uint(Ups[(k0 + t4) * SP + 8 * nt + g8]),
                                             __float_as_uint(Ups[(k0 + t4 + 4) * SP + 8 * nt + g8])};
-                    mma_tf32((ks & 1) ? cst2[nt] : cst[nt], a, bb);
+                    mma_tf32((ks & 1) ? cst2[nt] : st[nt], a, bb);
                 }
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int c = 8 * nt + 2 * t4;
-                St[m0 * SP + c] = cst[nt][0] + cst2[nt][0];
-                St[m0 * SP + c + 1] = cst[nt][1] + cst2[nt][1];
-                St[(m0 + 8) * SP + c] = cst[nt][2] + cst2[nt][2];
-                St[(m0 + 8) * SP + c + 1] = cst[nt][3] + cst2[nt][3];
+#pragma unroll
+                for (int f = 0; f < 4; ++f) st[nt][f] += cst2[nt][f];
+                St[m0 * SP + c] = tf32_round(st[nt][0]);
+                St[m0 * SP + c + 1] = tf32_round(st[nt][1]);
+                St[(m0 + 8) * SP + c] = tf32_round(st[nt][2]);
+                St[(m0 + 8) * SP + c + 1] = tf32_round(st[nt][3]);
             }
         }
-        __syncthreads();  // (C) S^T updated; this stage is free for block b+2
+        __syncthreads();  // (C) state copy updated; this stage is free for block b+2
     }
-    cp_async_wait<0>();
-    __syncthreads();
-    for (int e = t; e < D * DS; e += kThreads) Sg[(int64_t)(e / DS) * D + c0 + e % DS] = St[(e / DS) * SP + e % DS];
+
+    if (timed_out) {
+        // record the timeout, then wait (bounded) for this CTA's copies still in flight before leaving
+        if (t == 0) {
+            atomicOr(&g_gdn_device_error, 1u);
+            const int b = timed_out - 1;
+            if (!(b == 0 && p.debug_skip_first_copy)) mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
+            if (b + 1 < nb) mbar_wait_bounded(&bar[(b + 1) & 1], ((b + 1) >> 1) & 1, p.wait_limit);
+        }
+        __syncthreads();
+        return;
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int c = 8 * nt + 2 * t4;
+        if (owner) {
+            Sg[(int64_t)m0 * D + c0 + c] = st[nt][0];
+            Sg[(int64_t)m0 * D + c0 + c + 1] = st[nt][1];
+            Sg[(int64_t)(m0 + 8) * D + c0 + c] = st[nt][2];
+            Sg[(int64_t)(m0 + 8) * D + c0 + c + 1] = st[nt][3];
+        }
+    }
 }
 
 template <int D>
 static cudaError_t launch(const LaunchCommon &p, int64_t ch, cudaStream_t st) {
     constexpr int DS = kSliceCols, SP = DS + 8;
     constexpr size_t smem = sizeof(float) * (2 * (2 * kBlock * D + kBlock * D + 2 * kBlock * DS + 4) + D * SP +
-                                             kBlock * SP);
+                                             kBlock * SP) + 2 * sizeof(uint64_t);
     auto k = chain_tc_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -202,4 +255,13 @@ static cudaError_t launch(const LaunchCommon &p, int64_t ch, cudaStream_t st) {
 
 cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st) {
     return D == 64 ? gdn::launch<64>(p, ch, st) : gdn::launch<128>(p, ch, st);
+}
+
+cudaError_t gdn_take_device_error(unsigned int *out, cudaStream_t st) {
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(out, g_gdn_device_error, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    const unsigned int zero = 0;
+    return cudaMemcpyToSymbol(g_gdn_device_error, &zero, sizeof(unsigned int));
 }

@@ -33,7 +33,7 @@ GDN_MAX_SESSIONS = 4096
 EXPORTED = ["gdn_desc_tag", "gdn_desc_check", "gdn_state_bytes", "gdn_conv_state_bytes", "gdn_session_init",
             "gdn_workspace_size", "gdn_prefill_chunks", "gdn_prefill_varlen", "gdn_state_capture",
             "gdn_state_restore", "gdn_conv_state", "gdn_decode_step", "gdn_timing_begin", "gdn_timing_end",
-            "gdn_prefill_chunks_noalloc",
+            "gdn_prefill_chunks_noalloc", "gdn_device_status", "gdn_debug_inject_wait_timeout",
             "gdn_last_error", "gdn_status_string"]
 
 
@@ -94,6 +94,8 @@ def load_library(path: Optional[str] = None):
         "gdn_decode_step": (ctypes.c_int, [D, Sp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
         "gdn_timing_begin": (ctypes.c_int, [i32]),
         "gdn_timing_end": (ctypes.c_int, [ctypes.POINTER(gdn_kernel_time), i32, ctypes.POINTER(i32)]),
+        "gdn_device_status": (ctypes.c_int, [vp]),
+        "gdn_debug_inject_wait_timeout": (ctypes.c_int, [i32, i64]),
         "gdn_last_error": (ctypes.c_char_p, []),
         "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
@@ -273,3 +275,12 @@ def gdn_timing_end() -> dict:
     _check(load_library().gdn_timing_end(arr, 8, ctypes.byref(n)))
     return {arr[i].name.decode(): (int(arr[i].launches), int(arr[i].timed), float(arr[i].total_ms))
             for i in range(min(n.value, 8))}
+
+
+def gdn_device_status(stream=None) -> int:
+    """GDN_OK, or GDN_ERR_TIMEOUT if a kernel gave up a bounded wait since the last check (synchronises)."""
+    return int(load_library().gdn_device_status(_stream(stream)))
+
+
+def gdn_debug_inject_wait_timeout(enable: bool, wait_limit: int = 1000):
+    _check(load_library().gdn_debug_inject_wait_timeout(1 if enable else 0, wait_limit))

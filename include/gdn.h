@@ -212,6 +212,20 @@ typedef struct gdn_kernel_time {
 gdn_status gdn_timing_begin(int32_t max_launches);
 gdn_status gdn_timing_end(gdn_kernel_time *out, int32_t max_kinds, int32_t *n_kinds);
 
+/* Outcome of the device-side bounded waits. Kernels that wait on their own
+ * asynchronous operand copies give up after a bounded number of polls instead
+ * of hanging; they then record the fact in a device error word, leave their
+ * results incomplete and exit. This call synchronises `stream`, reads and
+ * clears that word, and returns GDN_ERR_TIMEOUT if it was set, else GDN_OK.
+ * (A timeout does not happen in normal operation.) */
+gdn_status gdn_device_status(gdn_stream_t stream);
+
+/* Test hook for the timeout path above: while enabled, prefill launches of the
+ * bf16 path never issue their first operand copy and give up after
+ * `wait_limit` polls, so the wait runs out without any fault. enable = 0
+ * restores normal operation. Process-global; for tests only. */
+gdn_status gdn_debug_inject_wait_timeout(int32_t enable, int64_t wait_limit);
+
 /* Message of the last failing call on this host thread ("" if none). */
 const char *gdn_last_error(void);
 

@@ -1,0 +1,39 @@
+"""The bounded-wait path of the state kernel, exercised without any fault.
+
+The state kernel waits on its own asynchronous operand copies with a bounded
+number of polls. The test hook makes a launch skip its first copy, so the wait
+runs out: the kernel must record the timeout, exit, and leave the context
+usable; gdn_device_status reports it once and then clears it."""
+import pytest
+import torch
+
+from chunked_gated_deltanet_gb300 import gdn
+from chunked_gated_deltanet_gb300 import workloads as wl
+from helpers import Runner
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_timeout_is_reported_and_context_survives(cuda_device):
+    shape = wl.Shape(2, 2, 128, 128, 64, wl.BF16)
+    w = wl.Workload("timeout", shape, seed=41, session_lengths=[256])
+    run = Runner(shape, w.session_tokens(0), w.conv_weights(), cuda_device)
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    victim, out = run.session(), run.new_out()
+    gdn.gdn_debug_inject_wait_timeout(True, 2000)
+    try:
+        run.prefill(victim, 0, 256, out)
+        status = gdn.gdn_device_status()
+    finally:
+        gdn.gdn_debug_inject_wait_timeout(False)
+    assert status == gdn.GDN_ERR_TIMEOUT
+    assert gdn.gdn_device_status() == gdn.GDN_OK          # reported once, then cleared
+    # the context still works and gives the same result as before
+    a, b = run.session(), run.session()
+    oa, ob = run.new_out(), run.new_out()
+    run.prefill(a, 0, 256, oa)
+    run.prefill(b, 0, 256, ob)
+    torch.cuda.synchronize()
+    assert gdn.gdn_device_status() == gdn.GDN_OK
+    assert torch.equal(oa, ob) and torch.equal(a.S, b.S)
+    assert torch.isfinite(oa).all()
