@@ -119,15 +119,17 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
     for (int b = 0; b < nb; ++b) {
         const float *buf = smem + (b & 1) * STAGE;
         if (t == 0 && b + 1 < nb) issue(b + 1);   // the other stage was released at the end of step b-1
-        const bool ok = mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
-        if (__syncthreads_or(!ok)) { timed_out = b + 1; break; }   // (A) uniform decision
+        // every thread acquires the stage itself; a timeout is acted on at the end of the step
+        if (!mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit)) timed_out = b + 1;
 
-        // Z = [W; Qe] S^T, two partial accumulators (even / odd k-steps) per n-tile
-        float acc[NT][4], acc2[NT][4];
+        // Z = [W; Qe] S^T, four partial accumulators per n-tile (k-step mod 4)
+        float acc[4][NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int f = 0; f < 4; ++f) acc[nt][f] = acc2[nt][f] = 0.f;
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int f = 0; f < 4; ++f) acc[j][nt][f] = 0.f;
         {
             const float4 *wa = reinterpret_cast<const float4 *>(buf) + (warp * (D / 8)) * 32 + lane;
 #pragma unroll
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint32_t bb[2] = {__float_as_uint(St[(k0 + t4) * SP + 8 * nt + g8]),
                                             __float_as_uint(St[(k0 + t4 + 4) * SP + 8 * nt + g8])};
-                    mma_tf32((ks & 1) ? acc2[nt] : acc[nt], a, bb);
+                    mma_tf32(acc[ks & 3][nt], a, bb);
                 }
             }
         }
@@ -152,8 +154,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const float4 u = uo[(w4 * NT + nt) * 32 + lane];
-                const float z[4] = {acc[nt][0] + acc2[nt][0], acc[nt][1] + acc2[nt][1], acc[nt][2] + acc2[nt][2],
-                                    acc[nt][3] + acc2[nt][3]};
+                float z[4];
+#pragma unroll
+                for (int f = 0; f < 4; ++f) z[f] = (acc[0][nt][f] + acc[1][nt][f]) + (acc[2][nt][f] + acc[3][nt][f]);
                 const int c = 8 * nt + 2 * t4, i = 16 * w4 + g8;
                 if (warp < 4) {
                     Ups[i * SP + c] = tf32_round(u.x - z[0]);
@@ -180,13 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
         // S^T <- e^{gamma_63} S^T + K_tilde^T U' on the owner warps' registers
         if (owner) {
             const float e = buf[WQF + KTF + 2 * UF];
-            float cst2[NT][4];
+            float cx[3][NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int f = 0; f < 4; ++f) {
                     st[nt][f] *= e;
-                    cst2[nt][f] = 0.f;
+                    cx[0][nt][f] = cx[1][nt][f] = cx[2][nt][f] = 0.f;
                 }
             const float4 *ka = reinterpret_cast<const float4 *>(buf + WQF) + (warp * 8) * 32 + lane;
 #pragma unroll
@@ -199,21 +202,25 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint32_t bb[2] = {__float_as_uint(Ups[(k0 + t4) * SP + 8 * nt + g8]),
                                             __float_as_uint(Ups[(k0 + t4 + 4) * SP + 8 * nt + g8])};
-                    mma_tf32((ks & 1) ? cst2[nt] : st[nt], a, bb);
+                    mma_tf32((ks & 3) ? cx[(ks & 3) - 1][nt] : st[nt], a, bb);
                 }
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int c = 8 * nt + 2 * t4;
 #pragma unroll
-                for (int f = 0; f < 4; ++f) st[nt][f] += cst2[nt][f];
+                for (int f = 0; f < 4; ++f) st[nt][f] += (cx[0][nt][f] + cx[1][nt][f]) + cx[2][nt][f];
                 St[m0 * SP + c] = tf32_round(st[nt][0]);
                 St[m0 * SP + c + 1] = tf32_round(st[nt][1]);
                 St[(m0 + 8) * SP + c] = tf32_round(st[nt][2]);
                 St[(m0 + 8) * SP + c + 1] = tf32_round(st[nt][3]);
             }
         }
-        __syncthreads();  // (C) state copy updated; this stage is free for block b+2
+        // (C) state copy updated; this stage is free for block b+2; uniform timeout decision
+        if (__syncthreads_or(timed_out)) {   // every thread leaves at the same step
+            timed_out = b + 1;
+            break;
+        }
     }
 
     if (timed_out) {
