@@ -239,10 +239,18 @@ def cpu_threads(n_heads: int) -> int:
     return max(1, min(c, n_heads))
 
 
-def traffic_record(kernel_file: str):
-    """Per-token DRAM bytes of the dominant kernel from the committed ncu summary, if the kernel is unchanged."""
-    src = os.path.join(ROOT, "chunked_gated_deltanet_gb300", "csrc", kernel_file)
-    prof = os.path.join(ROOT, "profiles", "state_output_qwen08b_replay.md")
+# kernel kind -> (source file, committed ncu summary) of the bf16 path
+PROFILED = {"prep_wy": ("prep_tc.cu", "prep_wy_qwen08b_replay.md"),
+            "state_output": ("chain_tc.cu", "state_output_qwen08b_replay.md")}
+
+
+def traffic_record(kind: str):
+    """DRAM bytes per token of a kernel from its committed ncu summary, if its source is unchanged since."""
+    if kind not in PROFILED:
+        return None
+    src_name, prof_name = PROFILED[kind]
+    src = os.path.join(ROOT, "chunked_gated_deltanet_gb300", "csrc", src_name)
+    prof = os.path.join(ROOT, "profiles", prof_name)
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         txt = open(prof).read()
@@ -339,7 +347,7 @@ def main():
     tokens_per_launch = step.tokens_per_step / prefill_launches
     achieved = bpt * tokens_per_launch / (avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peaks()
-    traffic_bpt = traffic_record("state.cu") if name == "state_output" else None
+    traffic_bpt = traffic_record(name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_src, "kernel": name,
                 "algorithmic_bytes_per_token": bpt, "tokens_per_launch": round(tokens_per_launch, 1),
