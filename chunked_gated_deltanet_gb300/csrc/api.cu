@@ -329,7 +329,8 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
             i0 = i;
             if (cnt == 0) continue;
             p.n_sess = cnt; p.nblk = blk;
-            cudaError_t e;
+            cudaError_t e = gdn_device_error_word(&p.err);
+            if (e != cudaSuccess) return cuda_fail(e, "device error word lookup");
             if (in_bf16) {
                 // bf16 inputs: tf32 tensor-core kernels; the state kernel also commits the conv state
                 e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep_tc(p, D, ch, cst); });

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
     if (timed_out) {
         // record the timeout, then wait (bounded) for this CTA's copies still in flight before leaving
         if (t == 0) {
-            atomicOr(&g_gdn_device_error, 1u);
+            atomicOr(p.err, 1u);
             const int b = timed_out - 1;
             if (!(b == 0 && p.debug_skip_first_copy)) mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
             if (b + 1 < nb) mbar_wait_bounded(&bar[(b + 1) & 1], ((b + 1) >> 1) & 1, p.wait_limit);
@@ -262,6 +262,26 @@ static cudaError_t launch(const LaunchCommon &p, int64_t ch, cudaStream_t st) {
 
 cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st) {
     return D == 64 ? gdn::launch<64>(p, ch, st) : gdn::launch<128>(p, ch, st);
+}
+
+#include <mutex>
+
+cudaError_t gdn_device_error_word(unsigned int **out) {
+    static std::mutex mu;
+    static unsigned int *addr[64] = {};
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *a = nullptr;
+        e = cudaGetSymbolAddress(&a, g_gdn_device_error);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<unsigned int *>(a);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t gdn_take_device_error(unsigned int *out, cudaStream_t st) {

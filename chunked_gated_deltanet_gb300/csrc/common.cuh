@@ -33,6 +33,7 @@ struct LaunchCommon {
     int n_sess;
     int nblk;                   // total blocks of this launch
     long long wait_limit;       // polls before a bounded mbarrier wait gives up
+    unsigned int *err;          // device error word (bit 0: a bounded wait ran out)
     int debug_skip_first_copy;  // test hook: never issue the first operand copy (the wait runs out)
     SessRef s[kLaunchSessions];
 };
@@ -90,6 +91,8 @@ __device__ __forceinline__ float conv_tap(const float w[4], float xm3, float xm2
 
 // Reads and clears the device error word after synchronising the stream (bit 0: a bounded wait ran out).
 cudaError_t gdn_take_device_error(unsigned int *out, cudaStream_t st);
+// Device address of the error word on the current device (looked up once per device).
+cudaError_t gdn_device_error_word(unsigned int **out);
 
 // Sets the message gdn_last_error() returns on this host thread (library-internal).
 void gdn_internal_set_error(const char *msg);
