@@ -240,19 +240,27 @@ def cpu_threads(n_heads: int) -> int:
 
 
 # kernel kind -> (source file, committed ncu summary) of the bf16 path
-PROFILED = {"prep_wy": ("prep_tc.cu", "prep_wy_qwen08b_replay.md"),
-            "state_output": ("chain_tc.cu", "state_output_qwen08b_replay.md")}
+# kernel kind -> (the sources that define its code, its ncu summary); the summary's figures are used only
+# while the sha256 over those sources matches the one it records
+PROFILED = {"prep_wy": (("prep_umma.cu", "umma.cuh", "mma.cuh", "common.cuh"), "prep_umma_qwen08b_replay.md"),
+            "state_output": (("chain_tc.cu", "mma.cuh", "common.cuh"), "state_output_qwen08b_replay.md")}
+
+
+def source_sha16(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "chunked_gated_deltanet_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def traffic_record(kind: str):
     """DRAM bytes per token of a kernel from its committed ncu summary, if its source is unchanged since."""
     if kind not in PROFILED:
         return None
-    src_name, prof_name = PROFILED[kind]
-    src = os.path.join(ROOT, "chunked_gated_deltanet_gb300", "csrc", src_name)
+    src_names, prof_name = PROFILED[kind]
     prof = os.path.join(ROOT, "profiles", prof_name)
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = source_sha16(src_names)
         txt = open(prof).read()
         m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", txt)
         m_b = re.search(r"dram_bytes_per_token:\s*([0-9.]+)", txt)

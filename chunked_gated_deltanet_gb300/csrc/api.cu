@@ -3,6 +3,8 @@
 #include "gdn.h"
 #include "common.cuh"
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
@@ -86,10 +88,17 @@ gdn_status check_state(const gdn_layer_desc *d, const gdn_session *s, const char
     return GDN_OK;
 }
 
-// Workspace layout for a launch of up to nblk blocks.
+// Workspace layout for a launch of up to nblk blocks. Offsets count from the workspace pointer
+// rounded up to 256 bytes (the kernels' widest stores want 32-byte alignment); `bytes` includes
+// that slack.
 struct WsLayout {
     size_t qk_off, wu_off, bytes;
 };
+constexpr size_t kWsAlign = 256;
+char *ws_base(void *workspace) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(workspace);
+    return reinterpret_cast<char *>((a + kWsAlign - 1) & ~(uintptr_t)(kWsAlign - 1));
+}
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -99,12 +108,12 @@ WsLayout ws_layout(const gdn_layer_desc *d, int64_t nblk) {
     if (d->in_dtype == GDN_BF16) {  // tensor-core path: one record per (block, v-head)
         L.qk_off = 0;
         L.wu_off = 0;
-        L.bytes = align256((size_t)nblk * d->n_v_heads * gdn::rec_floats(D) * sizeof(float));
+        L.bytes = kWsAlign + align256((size_t)nblk * d->n_v_heads * gdn::rec_floats(D) * sizeof(float));
         return L;
     }
     L.qk_off = 0;
     L.wu_off = align256((size_t)nblk * d->n_qk_heads * gdn::qk_floats(D) * sizeof(float));
-    L.bytes = L.wu_off + align256((size_t)nblk * d->n_v_heads * gdn::wu_floats(D) * sizeof(float));
+    L.bytes = kWsAlign + L.wu_off + align256((size_t)nblk * d->n_v_heads * gdn::wu_floats(D) * sizeof(float));
     return L;
 }
 
@@ -122,6 +131,28 @@ void fill_common(LaunchCommon &p, const gdn_layer_desc *d, const void *xq, const
     p.Hk = d->n_qk_heads; p.Hv = d->n_v_heads; p.G = d->n_v_heads / d->n_qk_heads;
     p.act = d->conv_act; p.out_bf16 = d->out_dtype == GDN_BF16;
     p.q_scale = d->q_scale; p.eps = d->l2_eps;
+}
+
+// 2-D tensor map over a row-major bf16 [rows][cols] input, boxes of 64 rows x 128 channels.
+// cuTensorMapEncodeTiled is reached through the runtime's driver entry point (no libcuda link).
+cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)std::max<int64_t>(rows, 1)};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {128, (cuuint32_t)kBlock};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 // ---- optional per-kernel event timing ----
@@ -315,8 +346,15 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
         static_assert(sizeof(LaunchCommon) <= 4096, "launch parameters must fit the 4 KB limit");
         LaunchCommon p;
         fill_common(p, d, xq, xk, xv, g, beta, conv_w, out);
-        p.ws_qk = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.qk_off);
-        p.ws_wu = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.wu_off);
+        p.ws_qk = reinterpret_cast<float *>(ws_base(workspace) + L.qk_off);
+        p.ws_wu = reinterpret_cast<float *>(ws_base(workspace) + L.wu_off);
+        if (in_bf16 && D == 128) {   // input tensor maps of the tcgen05 prologue
+            const int64_t rows = cu[n_sessions];
+            cudaError_t e = encode_rows_map(&p.tm_q, xq, rows, (int64_t)d->n_qk_heads * D);
+            if (e == cudaSuccess) e = encode_rows_map(&p.tm_k, xk, rows, (int64_t)d->n_qk_heads * D);
+            if (e == cudaSuccess) e = encode_rows_map(&p.tm_v, xv, rows, (int64_t)d->n_v_heads * D);
+            if (e != cudaSuccess) return cuda_fail(e, "input tensor-map encoding");
+        }
         for (int i0 = 0; i0 < n_sessions;) {
             int cnt = 0, i = i0, blk = 0;
             for (; i < n_sessions && cnt < gdn::kLaunchSessions; ++i) {
@@ -333,7 +371,7 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
             if (e != cudaSuccess) return cuda_fail(e, "device error word lookup");
             if (in_bf16) {
                 // bf16 inputs: tf32 tensor-core kernels; the state kernel also commits the conv state
-                e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep_tc(p, D, ch, cst); });
+                e = launch_k(K_PREP, cst, [&] { return D == 128 ? gdn_launch_prep_umma(p, ch, cst) : gdn_launch_prep_tc(p, D, ch, cst); });
                 if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
                 e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_tc(p, D, ch, cst); });
             } else {
@@ -474,7 +512,8 @@ GDN_API gdn_status gdn_debug_inject_wait_timeout(int32_t enable, int64_t wait_li
         return GDN_OK;
     }
     if (wait_limit < 1) return fail(GDN_ERR_INVALID_ARG, "wait_limit must be >= 1");
-    g_skip_first_copy = 1;
+    if (enable != 1 && enable != 2) return fail(GDN_ERR_INVALID_ARG, "enable must be 0, 1 or 2");
+    g_skip_first_copy = enable;
     g_wait_limit = wait_limit;
     return GDN_OK;
 }

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
         float *buf = smem + (b & 1) * STAGE;
         const float *r = p.ws_wu + ((int64_t)(s.blk0 + b) * Hv + h) * RF;
         uint64_t *br = &bar[b & 1];
-        if (b == 0 && p.debug_skip_first_copy) return;   // test hook: leave the barrier pending
+        if (b == 0 && p.debug_skip_first_copy == 1) return;   // test hook: leave the barrier pending
         fence_proxy_async();
         mbar_arrive_expect_tx(br, (uint32_t)sizeof(float) * (WQF + KTF + 2 * UF + 4));
         constexpr int CHUNK = 4096;   // floats per bulk copy (16 KB)
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
         if (t == 0) {
             atomicOr(p.err, 1u);
             const int b = timed_out - 1;
-            if (!(b == 0 && p.debug_skip_first_copy)) mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
+            if (!(b == 0 && p.debug_skip_first_copy == 1)) mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
             if (b + 1 < nb) mbar_wait_bounded(&bar[(b + 1) & 1], ((b + 1) >> 1) & 1, p.wait_limit);
         }
         __syncthreads();

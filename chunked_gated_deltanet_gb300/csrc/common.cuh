@@ -1,6 +1,7 @@
 // Internal definitions shared by the library's kernels and its C ABI layer.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,8 +35,11 @@ struct LaunchCommon {
     int nblk;                   // total blocks of this launch
     long long wait_limit;       // polls before a bounded mbarrier wait gives up
     unsigned int *err;          // device error word (bit 0: a bounded wait ran out)
-    int debug_skip_first_copy;  // test hook: never issue the first operand copy (the wait runs out)
+    int debug_skip_first_copy;  // test hook: 1 = the state kernel, 2 = the tcgen05 prologue never issues its first copy
     SessRef s[kLaunchSessions];
+    // 2-D tensor maps over xq [rows][Hk D], xk [rows][Hk D], xv [rows][Hv D] (bf16, boxes of 64 rows x 128
+    // channels) for the tcgen05 prologue's input copies; encoded by the host per call, unused elsewhere
+    CUtensorMap tm_q, tm_k, tm_v;
 };
 
 // Per-(block, v-head) record in the workspace: W [64][D], U [64][D], P [64][64], gamma [64].
@@ -101,6 +105,7 @@ void gdn_internal_set_error(const char *msg);
 cudaError_t gdn_launch_prep(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_state(const gdn::LaunchCommon &p, int D, cudaStream_t st);
 cudaError_t gdn_launch_prep_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
+cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *dst1, const void *src1,

@@ -1,0 +1,596 @@
+// Prologue + WY/UT transform on the 5th-generation tensor core (tcgen05,
+// accumulators in TMEM), bf16 inputs, d_k = d_v = 128. One CTA per (64-token
+// block, q/k head), for each of the head's G v-heads.
+//
+// The quantities are those of the mma.sync prologue (prep_tc.cu):
+//   conv (kernel 4, halo from the conv state at a call's first block), L2 norm
+//   gamma = cumulative log-decay in the block
+//   A_ij = beta_i e^{gamma_i - gamma_j} (K K^T)_ij (j < i),  T = (I + A)^{-1}
+//   W = T diag(beta e^gamma) K_hat,  U = T diag(beta) V
+//   P_ij = e^{gamma_i - gamma_j} (Q K^T)_ij (j <= i)
+//   Qe = diag(e^gamma) Q_hat - P W,  O_intra = P U,  K_tilde = diag(e^{gamma_63 - gamma_j}) K_hat
+// and the record goes out in the fragment order the state kernel reads.
+//
+// The products run as tcgen05 MMAs of M = 128, issued by one thread, each
+// with bf16 hi/lo operand pairs (hi*hi + hi*lo + lo*hi, about 16 significant
+// bits per operand, fp32 accumulation). P W = (P T) Bk and P U = (P T) Bv, so
+// stacking [T; P T] as the A operand gives all four 64 x 128 results of the
+// block in one product whose every accumulator row is used:
+//   [Q_hat; K_hat] K_hat^T               N = 64,  K = 128 -> TMEM columns 0..63 (kept for every v-head)
+//   P T                                  N = 64,  K = 64  -> TMEM columns 64..127 (rows 64..127 unused)
+//   [T; P T] [beta e^gamma K_hat | beta V] N = 256, K = 64 -> TMEM columns 256..511: [W U; P W P U]
+// Operands live in shared memory in the no-swizzle layouts of umma.cuh: the
+// row-ordered operands (q_hat, k_hat, P, T, P T) K-major, the token-by-channel
+// B operands MN-major, so that every producer writes whole 16-byte
+// core-matrix rows. The triangular inverse stays in fp32 on the CUDA cores.
+// The input tiles arrive as 2-D tensor copies (one per tile) plus three
+// single-row halo copies, on an mbarrier; every wait is bounded, and on a
+// timeout the CTA records it in the device error word, waits (bounded) for
+// what it has in flight, frees its TMEM and returns.
+#include "common.cuh"
+#include "mma.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+constexpr int kUmmaPrepThreads = 512;
+
+namespace up {   // shared-memory plan, bytes
+constexpr int D = 128;
+constexpr uint32_t AQ_LBO = 144, AQ_SBO = 16 * AQ_LBO;    // [q_hat; k_hat], K-major, K = 128, 16-byte gap between K cores
+constexpr uint32_t AQ_BYTES = 16 * AQ_SBO;                  // 128 rows
+constexpr uint32_t B_LBO = 128, B_SBO = 8 * B_LBO + 16;     // [beta e^gamma k_hat | beta v], MN-major, N = 256, K = 64
+constexpr uint32_t B_BYTES = 32 * B_SBO;
+constexpr uint32_t K64_LBO = 128, K64_SBO = 8 * K64_LBO;    // K = 64 operands: P, [T; P T] (K-major), T (MN-major)
+constexpr uint32_t R64_BYTES = 8 * K64_SBO;                 // 64 rows (or 64 columns) of a K = 64 operand
+constexpr int LT = kBlock + 4;                              // fp32 A and T row pitch (floats)
+constexpr uint32_t OFF_AQH = 0, OFF_AQL = AQ_BYTES;
+constexpr uint32_t OFF_BH = 2 * AQ_BYTES, OFF_BL = OFF_BH + B_BYTES;
+constexpr uint32_t OFF_PH = OFF_BL + B_BYTES, OFF_PL = OFF_PH + R64_BYTES;     // P, K-major
+constexpr uint32_t OFF_TBH = OFF_PL + R64_BYTES, OFF_TBL = OFF_TBH + R64_BYTES; // T, MN-major (B of P T)
+constexpr uint32_t OFF_AF = OFF_TBL + R64_BYTES;             // fp32 A (input of the inverse)
+constexpr uint32_t OFF_TF = OFF_AF + 4 * kBlock * LT;        // fp32 T
+constexpr uint32_t OFF_MT = OFF_TF + 4 * kBlock * LT;        // 3 x 16 x 17 inverse scratch
+constexpr uint32_t OFF_ATH = OFF_AF, OFF_ATL = OFF_ATH + 2 * R64_BYTES;   // [T; P T], K-major, over A and T
+constexpr uint32_t OFF_SMALL = OFF_MT + 4 * 3 * 16 * 17;     // gamma, beta, e^gamma
+constexpr uint32_t W_BYTES = D * 4 * 2;                      // conv weights of one head's channels (bf16 [D][4])
+constexpr uint32_t OFF_W = OFF_SMALL + 4 * 3 * kBlock;       // q, k, v conv weights
+constexpr uint32_t OFF_BAR = OFF_W + 3 * W_BYTES;            // [0] input copies, [1] MMA groups; TMEM slot
+constexpr uint32_t SMEM = OFF_BAR + 32;
+constexpr uint32_t RAW_ROW = 2 * D, RAW_TILE = (kBlock + 3) * RAW_ROW;
+constexpr uint32_t TILE_TX = RAW_TILE + W_BYTES;               // bytes one staged tile brings in
+constexpr uint32_t OFF_RAW = OFF_PH;                         // raw input tiles: dead before P, T, A are written
+static_assert(OFF_RAW + 3 * RAW_TILE <= OFF_SMALL, "raw tiles must fit the P, T and inverse regions");
+static_assert(OFF_ATL + 2 * R64_BYTES <= OFF_MT, "[T; P T] must fit over A and T");
+static_assert(OFF_RAW % 128 == 0 && RAW_TILE % 128 == 0, "tensor-copy destinations 128-byte aligned");
+// the P T product reads 128 A rows from P's low half: the 64 rows after it are T's, in bounds
+static_assert(OFF_PL + 2 * R64_BYTES <= SMEM, "rows read past P's low part");
+static_assert(SMEM <= 227 * 1024, "shared memory");
+}  // namespace up
+
+// dst[0] = a, dst[1] = b in one 32-byte store (dst 32-byte aligned)
+__device__ __forceinline__ void st_v8(float4 *dst, float4 a, float4 b) {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"l"(dst), "f"(a.x), "f"(a.y), "f"(a.z), "f"(a.w),
+                 "f"(b.x), "f"(b.y), "f"(b.z), "f"(b.w)
+                 : "memory");
+}
+
+// Each thread of a warp holds row r (r % 16 == lane % 16) of a 16-column chunk
+// starting at column c0 (a multiple of 16). The pair of lanes (l, l ^ 8)
+// holds rows r and r ^ 8 and together writes their m16n8k8 A fragments
+// (float4 per fragment lane) of an operand with K columns: each thread the
+// two adjacent fragment lanes L, L + 1 (L even) in one 32-byte store, so that a
+// store instruction fills whole sectors.
+__device__ __forceinline__ void put_afrag16(float *base, int r, int c0, const float (&v)[16], int K, int lane) {
+    const bool upper = lane & 8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float *w = v + 8 * h;
+        const float p0 = __shfl_xor_sync(0xffffffffu, upper ? w[0] : w[2], 8);
+        const float p1 = __shfl_xor_sync(0xffffffffu, upper ? w[1] : w[3], 8);
+        const float p2 = __shfl_xor_sync(0xffffffffu, upper ? w[4] : w[6], 8);
+        const float p3 = __shfl_xor_sync(0xffffffffu, upper ? w[5] : w[7], 8);
+        const float4 f0 = upper ? make_float4(p0, w[2], p2, w[6]) : make_float4(w[0], p0, w[4], p2);
+        const float4 f1 = upper ? make_float4(p1, w[3], p3, w[7]) : make_float4(w[1], p1, w[5], p3);
+        const int L = 4 * (r & 7) + (upper ? 2 : 0), ks = (c0 >> 3) + h;
+        float4 *dst = reinterpret_cast<float4 *>(base) + (((r >> 4) * (K >> 3) + ks) * 32 + L);
+        st_v8(dst, f0, f1);
+    }
+}
+
+// Same pairing, for row i of a 64 x D accumulator stored by 16-column slices
+// of m16n8 C fragments (cfrag_slice_index order).
+__device__ __forceinline__ void put_cfrag16(float *base, int i, int c0, const float (&v)[16], int lane) {
+    const bool upper = lane & 8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float *w = v + 8 * h;
+        const float p0 = __shfl_xor_sync(0xffffffffu, upper ? w[0] : w[4], 8);
+        const float p1 = __shfl_xor_sync(0xffffffffu, upper ? w[1] : w[5], 8);
+        const float p2 = __shfl_xor_sync(0xffffffffu, upper ? w[2] : w[6], 8);
+        const float p3 = __shfl_xor_sync(0xffffffffu, upper ? w[3] : w[7], 8);
+        const float4 f0 = upper ? make_float4(p0, p1, w[4], w[5]) : make_float4(w[0], w[1], p0, p1);
+        const float4 f1 = upper ? make_float4(p2, p3, w[6], w[7]) : make_float4(w[2], w[3], p2, p3);
+        const int L = 4 * (i & 7) + (upper ? 2 : 0);
+        float4 *dst = reinterpret_cast<float4 *>(base) + ((((c0 >> 4) * 4 + (i >> 4)) * 2 + h) * 32 + L);
+        st_v8(dst, f0, f1);
+    }
+}
+
+// 8 fp32 values -> bf16 hi and lo halves, packed for one 16-byte core-matrix row each
+__device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        __nv_bfloat16 h0, l0, h1, l1;
+        split_bf16(v[2 * q], h0, l0);
+        split_bf16(v[2 * q + 1], h1, l1);
+        h[q] = pack_bf16(h0, h1);
+        l[q] = pack_bf16(l0, l1);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// hi + lo of 8 bf16 pairs (one core-matrix row of each half)
+__device__ __forceinline__ void join8(uint4 hi, uint4 lo, float *v) {
+    const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w}, l[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = __uint_as_float(h[q] << 16) + __uint_as_float(l[q] << 16);
+        v[2 * q + 1] = __uint_as_float(h[q] & 0xFFFF0000u) + __uint_as_float(l[q] & 0xFFFF0000u);
+    }
+}
+
+__global__ void __launch_bounds__(kUmmaPrepThreads, 1)
+    prep_umma_kernel(const __grid_constant__ LaunchCommon p, int64_t ch) {
+    using namespace up;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    unsigned char *AQh = sm + OFF_AQH, *AQl = sm + OFF_AQL, *Bh = sm + OFF_BH, *Bl = sm + OFF_BL;
+    unsigned char *Ph = sm + OFF_PH, *Pl = sm + OFF_PL, *TBh = sm + OFF_TBH, *TBl = sm + OFF_TBL;
+    unsigned char *ATh = sm + OFF_ATH, *ATl = sm + OFF_ATL;
+    float *Af = reinterpret_cast<float *>(sm + OFF_AF), *Tf = reinterpret_cast<float *>(sm + OFF_TF);
+    float *Mt = reinterpret_cast<float *>(sm + OFF_MT);
+    float *gam = reinterpret_cast<float *>(sm + OFF_SMALL), *bet = gam + kBlock, *egv = bet + kBlock;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 2);
+    __nv_bfloat16 *rawq = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_RAW);
+    __nv_bfloat16 *rawk = rawq + (kBlock + 3) * D, *rawv = rawk + (kBlock + 3) * D;
+    __nv_bfloat16 *wq = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W), *wk = wq + 4 * D, *wv = wk + 4 * D;
+
+    const int blk = blockIdx.x, hk = blockIdx.y, t = threadIdx.x;
+    const int warp = t >> 5, lane = t & 31;
+    const SessRef s = p.s[find_session(p, blk)];
+    const int pos0 = (blk - s.blk0) * kBlock;
+    const int n = min(kBlock, s.n - pos0);
+    const int64_t row0 = s.row0 + pos0;
+    const int Hk = p.Hk, Hv = p.Hv;
+    const int64_t nq = (int64_t)Hk * D, nv = (int64_t)Hv * D;
+    const __nv_bfloat16 *cw = static_cast<const __nv_bfloat16 *>(p.conv_w);
+    const __nv_bfloat16 *cs = static_cast<const __nv_bfloat16 *>(s.conv);
+
+    if (warp == 0) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    if (t == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init_fence();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    uint32_t in_phase = 0, mma_phase = 0;
+    int in_pending = 0, mma_pending = 0;   // an issued copy group / MMA group not yet seen complete (CTA-uniform)
+
+    // Stage rows pos0-3 .. pos0+63 of `ntile` head tiles: one tensor copy of the block's 64 rows (rows past
+    // the inputs read as zero, rows past n belong to other tokens and only reach masked results) and three
+    // halo rows, from the inputs or, before a call's first token, from the conv state.
+    struct Tile { __nv_bfloat16 *dst, *wdst; const CUtensorMap *map; const __nv_bfloat16 *x; int64_t ld, col0, chan0; };
+    auto stage = [&](const Tile *tl, int ntile, bool skip) {
+        if (warp == 0 && !skip) {
+            if (lane == 0) mbar_arrive_expect_tx(&bar[0], (uint32_t)ntile * TILE_TX);
+            __syncwarp();
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                if (q >= ntile) break;
+                if (lane == 30) tma_load_2d(tl[q].dst + 3 * D, tl[q].map, (int)tl[q].col0, (int)row0, &bar[0]);
+                if (lane == 31) bulk_g2s(tl[q].wdst, cw + tl[q].chan0 * 4, W_BYTES, &bar[0]);
+                if (lane >= 3 * q && lane < 3 * q + 3) {
+                    const int r = lane - 3 * q, pos = pos0 - 3 + r;
+                    const __nv_bfloat16 *src =
+                        pos < 0 ? cs + (int64_t)(3 + pos) * ch + tl[q].chan0 : tl[q].x + (s.row0 + pos) * tl[q].ld + tl[q].col0;
+                    bulk_g2s(tl[q].dst + r * D, src, RAW_ROW, &bar[0]);
+                }
+            }
+        }
+        in_pending = 1;
+    };
+    // every thread waits; true when the phase completed for all of them (CTA-uniform)
+    auto wait_in = [&]() {
+        const bool ok = mbar_wait_bounded(&bar[0], in_phase, p.wait_limit);
+        if (__syncthreads_or(!ok)) return false;
+        in_phase ^= 1u;
+        in_pending = 0;
+        return true;
+    };
+    auto wait_mma = [&]() {
+        const bool ok = mbar_wait_bounded(&bar[1], mma_phase, p.wait_limit);
+        if (__syncthreads_or(!ok)) return false;
+        mma_phase ^= 1u;
+        mma_pending = 0;
+        tc_fence_after();
+        return true;
+    };
+    // bf16 hi/lo MMA group D (+)= A B over K (3 passes per 16-wide K-step), then a commit; thread 0 only
+    auto mma3 = [&](uint32_t d, uint64_t ah, uint64_t al, uint32_t astep, uint64_t bh, uint64_t bl, uint32_t bstep,
+                    int K, uint32_t id) {
+        tc_fence_after();
+        for (int ks = 0; ks < K / 16; ++ks) {
+            const uint64_t oa = (astep * ks) >> 4, ob = (bstep * ks) >> 4;
+            umma_bf16(d, ah + oa, bh + ob, id, ks > 0);
+            umma_bf16(d, ah + oa, bl + ob, id, 1);
+            umma_bf16(d, al + oa, bh + ob, id, 1);
+        }
+        umma_commit(&bar[1]);
+    };
+
+    // Row-parallel conv of rows [r0, r0 + nr) of a staged tile: lane owns channels 4 lane .. 4 lane + 3,
+    // four rows at a time; outputs go through emit(i0, y[4][4]).
+    auto conv_rows = [&](const __nv_bfloat16 *raw, const __nv_bfloat16 *wsm, int r0, int nr, auto &&emit) {
+        float w[4][4];
+        {
+            const uint4 u0 = *reinterpret_cast<const uint4 *>(wsm + lane * 16);
+            const uint4 u1 = *reinterpret_cast<const uint4 *>(wsm + lane * 16 + 8);
+            const uint32_t ww[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                w[e >> 1][2 * (e & 1)] = __uint_as_float(ww[e] << 16);
+                w[e >> 1][2 * (e & 1) + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+            }
+        }
+        for (int i0 = r0; i0 < r0 + nr; i0 += 4) {
+            float x[7][4];   // raw rows i0 .. i0+6 = block rows i0-3 .. i0+3
+#pragma unroll
+            for (int r = 0; r < 7; ++r) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(raw + (i0 + r) * D + lane * 4);
+                const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+                x[r][0] = __low2float(a); x[r][1] = __high2float(a); x[r][2] = __low2float(b); x[r][3] = __high2float(b);
+            }
+            float y[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    y[u][c] = conv_tap<__nv_bfloat16>(w[c], x[u][c], x[u + 1][c], x[u + 2][c], x[u + 3][c], p.act);
+            emit(i0, y);
+        }
+    };
+    auto split4_store = [&](unsigned char *hi, unsigned char *lo, uint32_t off, const float (&v)[4]) {
+        __nv_bfloat16 h[4], l[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) split_bf16(v[c], h[c], l[c]);
+        *reinterpret_cast<uint2 *>(hi + off) = make_uint2(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]));
+        *reinterpret_cast<uint2 *>(lo + off) = make_uint2(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]));
+    };
+    auto store8 = [&](unsigned char *hi, unsigned char *lo, uint32_t off, const float *v) {
+        uint4 h, l;
+        split8(v, h, l);
+        *reinterpret_cast<uint4 *>(hi + off) = h;
+        *reinterpret_cast<uint4 *>(lo + off) = l;
+    };
+
+    {   // 1. q, k and the first v-head's tiles
+        const Tile tl[3] = {
+            {rawq, wq, &p.tm_q, static_cast<const __nv_bfloat16 *>(p.xq), nq, (int64_t)hk * D, (int64_t)hk * D},
+            {rawk, wk, &p.tm_k, static_cast<const __nv_bfloat16 *>(p.xk), nq, (int64_t)hk * D, nq + (int64_t)hk * D},
+            {rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)(hk * p.G) * D, 2 * nq + (int64_t)(hk * p.G) * D}};
+        stage(tl, 3, p.debug_skip_first_copy == 2);
+    }
+    // g and beta of the first v-head (warps 2 and 3 own the gamma scan; warp 0 issues the MMAs)
+    const int jg = t - 64;
+    float gv = 0.f, bv = 0.f;
+    if (jg >= 0 && jg < n) {
+        gv = p.g[(row0 + jg) * Hv + hk * p.G];
+        bv = p.beta[(row0 + jg) * Hv + hk * p.G];
+    }
+    bool ok = wait_in();
+
+    if (ok) {
+        // 2. conv + L2 norm of q (warps 0-7) and k (warps 8-15), 8 rows per warp -> bf16 hi/lo rows of [q_hat; k_hat]
+        const int which = warp >> 3;
+        const float qs = which ? 1.f : p.q_scale;
+        conv_rows(which ? rawk : rawq, which ? wk : wq, 8 * (warp & 7), 8, [&](int i0, float (&y)[4][4]) {
+            float ss[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                ss[u] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ss[u] = fmaf(y[u][c], y[u][c], ss[u]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                const float scale = qs * rsqrtf(ss[u] + p.eps);
+                float v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = i < n ? y[u][c] * scale : 0.f;
+                split4_store(AQh, AQl, kmajor_bf16_offset(64 * which + i, 4 * lane, AQ_LBO, AQ_SBO), v);
+            }
+        });
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        // 3. [Q K^T; K K^T] = [q_hat; k_hat] k_hat^T into TMEM columns 0..63
+        if (t == 0)
+            mma3(tmem, umma_smem_desc(AQh, AQ_LBO, AQ_SBO), umma_smem_desc(AQl, AQ_LBO, AQ_SBO), 2 * AQ_LBO,
+                 umma_smem_desc(AQh + 8 * AQ_SBO, AQ_LBO, AQ_SBO), umma_smem_desc(AQl + 8 * AQ_SBO, AQ_LBO, AQ_SBO),
+                 2 * AQ_LBO, D, umma_idesc_bf16(128, 64, 0, 0));
+        mma_pending = 1;
+    }
+
+    // 4. each v-head of the group
+    for (int gi = 0; ok && gi < p.G; ++gi) {
+        const int h = hk * p.G + gi;
+        if (gi > 0) {   // the previous head is done with the raw-tile region and every MMA operand
+            const Tile tl[1] = {{rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)h * D, 2 * nq + (int64_t)h * D}};
+            stage(tl, 1, false);
+            gv = bv = 0.f;
+            if (jg >= 0 && jg < n) {
+                gv = p.g[(row0 + jg) * Hv + h];
+                bv = p.beta[(row0 + jg) * Hv + h];
+            }
+        }
+        if (jg >= 0 && jg < kBlock) {   // gamma: inclusive scan of g (warps 2 and 3)
+            float sv = gv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, sv, o);
+                if (lane >= o) sv += y;
+            }
+            gam[jg] = sv;
+            bet[jg] = bv;
+        }
+        if (gi > 0) {
+            if (!(ok = wait_in())) break;
+        } else {
+            __syncthreads();
+        }
+        if (jg >= 32 && jg < kBlock) gam[jg] += gam[31];
+        __syncthreads();
+        if (jg >= 0 && jg < kBlock) egv[jg] = expf(gam[jg]);
+        __syncthreads();
+        float *rec = p.ws_wu + ((int64_t)blk * Hv + h) * rec_floats(D);
+
+        // 5. B operand, MN-major: channels 128..255 = beta v (row-parallel conv, 4 rows per warp),
+        //    channels 0..127 = beta e^gamma k_hat (from the hi/lo rows)
+        conv_rows(rawv, wv, 4 * warp, 4, [&](int i0, float (&y)[4][4]) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                float v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = i < n ? bet[i] * y[u][c] : 0.f;
+                split4_store(Bh, Bl, mnmajor_bf16_offset(128 + 4 * lane, i, B_LBO, B_SBO), v);
+            }
+        });
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int j = t & 63, cg = (t >> 6) + 8 * it;
+            const uint32_t o = kmajor_bf16_offset(64 + j, 8 * cg, AQ_LBO, AQ_SBO);
+            float v[8];
+            join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), v);
+            const float sc = bet[j] * egv[j];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v[c] *= sc;
+            store8(Bh, Bl, mnmajor_bf16_offset(8 * cg, j, B_LBO, B_SBO), v);
+        }
+        fence_proxy_async();
+        if (gi == 0) {
+            if (!(ok = wait_mma())) break;   // Q K^T / K K^T landed in TMEM
+        } else {
+            __syncthreads();
+        }
+
+        // 6. from TMEM: P (rows 0..63 -> bf16 hi/lo K-major) and A (rows 64..127 -> fp32)
+        {
+            const int q = warp & 3, cp = warp >> 2, R = 32 * q + lane, j0 = 16 * cp;
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + j0, v);
+            if (R < kBlock) {
+                const int i = R;
+                float pv[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) pv[jj] = (j0 + jj) <= i ? v[jj] * __expf(gam[i] - gam[j0 + jj]) : 0.f;
+                store8(Ph, Pl, kmajor_bf16_offset(i, j0, K64_LBO, K64_SBO), pv);
+                store8(Ph, Pl, kmajor_bf16_offset(i, j0 + 8, K64_LBO, K64_SBO), pv + 8);
+            } else {
+                const int i = R - kBlock;
+                float av[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) av[jj] = (j0 + jj) < i ? bet[i] * __expf(gam[i] - gam[j0 + jj]) * v[jj] : 0.f;
+#pragma unroll
+                for (int c = 0; c < 16; c += 4)
+                    *reinterpret_cast<float4 *>(Af + i * LT + j0 + c) = make_float4(av[c], av[c + 1], av[c + 2], av[c + 3]);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // 7. T = (I + A)^{-1} in fp32: diagonal 16x16 blocks by substitution, one column per thread
+        if (t < kBlock) {
+            const int d = t >> 4, c = t & 15;
+            const float *Ad = Af + 16 * d * LT + 16 * d;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float sum = 0.f;
+#pragma unroll
+                for (int j = 0; j < i; ++j)
+                    if (j >= c) sum = fmaf(Ad[i * LT + j], x[j], sum);
+                x[i] = i < c ? 0.f : (i == c ? 1.f : -sum);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tf[(16 * d + i) * LT + 16 * d + c] = x[i];
+        }
+        __syncthreads();
+        //    off-diagonal blocks by distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+        for (int dist = 1; dist < 4; ++dist) {
+            const int nblkd = 4 - dist;
+            for (int e = t; e < nblkd * 256; e += kUmmaPrepThreads) {
+                const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15, ib = jb + dist;
+                float sum = 0.f;
+                for (int k = 16 * jb; k < 16 * ib; ++k) sum = fmaf(Af[(16 * ib + r) * LT + k], Tf[k * LT + 16 * jb + c], sum);
+                Mt[(jb * 16 + r) * 17 + c] = sum;
+            }
+            __syncthreads();
+            for (int e = t; e < nblkd * 256; e += kUmmaPrepThreads) {
+                const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15, ib = jb + dist;
+                float sum = 0.f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) sum = fmaf(Tf[(16 * ib + r) * LT + 16 * ib + k], Mt[(jb * 16 + k) * 17 + c], sum);
+                Tf[(16 * ib + r) * LT + 16 * jb + c] = -sum;
+            }
+            __syncthreads();
+        }
+        //    T as bf16 hi/lo: rows 0..63 of [T; P T] (K-major, written over A and T) and the B operand of
+        //    P T (MN-major); blocks above the diagonal are zero
+        {
+            const int i = t & 63, kg = t >> 6;
+            float v[8];
+            if ((kg >> 1) > (i >> 4)) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) v[c] = 0.f;
+            } else {
+                const float4 a = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg);
+                const float4 b = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg + 4);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            }
+            __syncthreads();   // every row of T is read before the first write over it
+            store8(ATh, ATl, kmajor_bf16_offset(i, 8 * kg, K64_LBO, K64_SBO), v);
+            store8(TBh, TBl, mnmajor_bf16_offset(8 * kg, i, K64_LBO, K64_SBO), v);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+
+        // 8. P T into TMEM columns 64..127; meanwhile K_tilde^T as tf32 A fragments (D x 64) and e^{gamma_63}
+        if (t == 0)
+            mma3(tmem + 64, umma_smem_desc(Ph, K64_LBO, K64_SBO), umma_smem_desc(Pl, K64_LBO, K64_SBO), 2 * K64_LBO,
+                 umma_smem_desc(TBh, K64_LBO, K64_SBO), umma_smem_desc(TBl, K64_LBO, K64_SBO), 2 * K64_LBO, kBlock,
+                 umma_idesc_bf16(128, 64, 0, 1));
+        mma_pending = 1;
+        if (warp > 0) {
+            const float gl = gam[kBlock - 1];
+            for (int e = t - 32; e < (D / 16) * 8 * 32; e += kUmmaPrepThreads - 32) {
+                const int ln = e & 31, tile = e >> 5, mt = tile >> 3, ks = tile & 7, gg = ln >> 2, tt = ln & 3;
+                float v[4];
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    const int m = 16 * mt + gg + 8 * (f & 1), k = 8 * ks + tt + 4 * (f >> 1);
+                    const uint32_t o = kmajor_bf16_offset(kBlock + k, m, AQ_LBO, AQ_SBO);
+                    const float kh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQh + o)) +
+                                     __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQl + o));
+                    v[f] = tf32_round(__expf(gl - gam[k]) * kh);
+                }
+                *reinterpret_cast<float4 *>(rec + 128 * D + e * 4) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+            if (t == 32) rec[320 * D] = expf(gl);
+        }
+        if (!(ok = wait_mma())) break;
+
+        // 9. P T (lanes 0..63; warps 0,1,4,5,8,9,12,13, 16 columns each) -> rows 64..127 of [T; P T]
+        if ((warp & 3) < 2) {
+            const int i = 32 * (warp & 3) + lane, c0 = 16 * (warp >> 2);
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 + c0, v);
+            store8(ATh, ATl, kmajor_bf16_offset(kBlock + i, c0, K64_LBO, K64_SBO), v);
+            store8(ATh, ATl, kmajor_bf16_offset(kBlock + i, c0 + 8, K64_LBO, K64_SBO), v + 8);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+
+        // 10. [W U; P W P U] = [T; P T] [beta e^gamma k_hat | beta v] into TMEM columns 256..511
+        if (t == 0)
+            mma3(tmem + 256, umma_smem_desc(ATh, K64_LBO, K64_SBO), umma_smem_desc(ATl, K64_LBO, K64_SBO), 2 * K64_LBO,
+                 umma_smem_desc(Bh, B_LBO, B_SBO), umma_smem_desc(Bl, B_LBO, B_SBO), 2 * B_LBO, kBlock,
+                 umma_idesc_bf16(128, 256, 0, 1));
+        mma_pending = 1;
+        if (!(ok = wait_mma())) break;
+
+        // 11. the record, every warp (lanes 32 (warp % 4) .., 64 columns at 64 (warp / 4)):
+        //     W rows -> tf32 A fragments (rows 0..63 of [W; Qe]); U rows -> C fragments;
+        //     P W rows -> Qe = e^gamma q_hat - P W (rows 64..127 of [W; Qe]); P U rows -> O_intra C fragments
+        {
+            const int R = 32 * (warp & 3) + lane, cp = warp >> 2;
+            const bool top = R < kBlock;
+            const int i = top ? R : R - kBlock;
+            const uint32_t tb = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 + 64 * cp;
+            uint32_t ra[16], rb[16];   // chunk cc in one, chunk cc + 1 in flight into the other
+            tmem_ld16_nowait(tb, ra);
+            tmem_wait_ld(ra);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t(&cur)[16] = (cc & 1) ? rb : ra;
+                uint32_t(&nxt)[16] = (cc & 1) ? ra : rb;
+                if (cc < 3) tmem_ld16_nowait(tb + 16 * (cc + 1), nxt);
+                const int c0 = 64 * cp + 16 * cc;
+                float v[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(cur[c]);
+                if (c0 < D) {
+                    if (top) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) v[c] = tf32_round(v[c]);
+                    } else {
+                        float qh[16];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const uint32_t o = kmajor_bf16_offset(i, c0 + 8 * hh, AQ_LBO, AQ_SBO);
+                            join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), qh + 8 * hh);
+                        }
+                        const float e = egv[i];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) v[c] = tf32_round(e * qh[c] - v[c]);
+                    }
+                    put_afrag16(rec, R, c0, v, D, lane);
+                } else {
+                    put_cfrag16(rec + (top ? 192 : 256) * D, i, c0 - D, v, lane);
+                }
+                if (cc < 3) tmem_wait_ld(nxt);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();   // TMEM columns and every operand region are free for the next v-head
+    }
+
+    if (!ok) {   // a bounded wait ran out: record it and wait (bounded) for what is still in flight
+        if (t == 0) {
+            atomicOr(p.err, 1u);
+            if (in_pending && p.debug_skip_first_copy != 2) mbar_wait_bounded(&bar[0], in_phase, p.wait_limit);
+            if (mma_pending) mbar_wait_bounded(&bar[1], mma_phase, p.wait_limit);
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace gdn
+
+cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st) {
+    using namespace gdn;
+    cudaError_t e = cudaFuncSetAttribute(prep_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)up::SMEM);
+    if (e != cudaSuccess) return e;
+    prep_umma_kernel<<<dim3(p.nblk, p.Hk), kUmmaPrepThreads, up::SMEM, st>>>(p, ch);
+    return cudaGetLastError();
+}

@@ -282,5 +282,6 @@ def gdn_device_status(stream=None) -> int:
     return int(load_library().gdn_device_status(_stream(stream)))
 
 
-def gdn_debug_inject_wait_timeout(enable: bool, wait_limit: int = 1000):
-    _check(load_library().gdn_debug_inject_wait_timeout(1 if enable else 0, wait_limit))
+def gdn_debug_inject_wait_timeout(enable: int, wait_limit: int = 1000):
+    """enable: 0 off, 1 the state kernel, 2 the tcgen05 prologue skips its first copy."""
+    _check(load_library().gdn_debug_inject_wait_timeout(int(enable), wait_limit))

@@ -107,8 +107,10 @@ gdn_status gdn_session_init(const gdn_layer_desc *desc, gdn_session *session, fl
                             void *conv, gdn_stream_t stream);
 
 /* Workspace bytes a prefill call needs for up to `max_tokens` tokens in total
- * over up to `max_sessions` sessions. Scratch of one call: its contents are
- * not needed afterwards, and calls that overlap on the GPU must not share it. */
+ * over up to `max_sessions` sessions, for any 16-byte-aligned workspace pointer
+ * (the size includes room for the library to align it further). Scratch of
+ * one call: its contents are not needed afterwards, and calls that overlap on
+ * the GPU must not share it. */
 size_t gdn_workspace_size(const gdn_layer_desc *desc, int64_t max_tokens, int32_t max_sessions);
 
 /* Prefill of one session.
@@ -221,9 +223,11 @@ gdn_status gdn_timing_end(gdn_kernel_time *out, int32_t max_kinds, int32_t *n_ki
 gdn_status gdn_device_status(gdn_stream_t stream);
 
 /* Test hook for the timeout path above: while enabled, prefill launches of the
- * bf16 path never issue their first operand copy and give up after
- * `wait_limit` polls, so the wait runs out without any fault. enable = 0
- * restores normal operation. Process-global; for tests only. */
+ * bf16 path give up after `wait_limit` polls, and one kernel never issues its
+ * first operand copy, so its wait runs out without any fault: enable = 1, the
+ * state kernel; enable = 2, the tcgen05 prologue (d_k = d_v = 128). enable = 0
+ * restores normal operation; other values are refused with
+ * GDN_ERR_INVALID_ARG. Process-global; for tests only. */
 gdn_status gdn_debug_inject_wait_timeout(int32_t enable, int64_t wait_limit);
 
 /* Message of the last failing call on this host thread ("" if none). */

@@ -1,8 +1,9 @@
-"""The bounded-wait path of the state kernel, exercised without any fault.
+"""The bounded-wait paths of the bf16 kernels, exercised without any fault.
 
-The state kernel waits on its own asynchronous operand copies with a bounded
-number of polls. The test hook makes a launch skip its first copy, so the wait
-runs out: the kernel must record the timeout, exit, and leave the context
+The state kernel and the tcgen05 prologue wait on their own asynchronous
+operand copies with a bounded number of polls. The test hook makes one of them
+skip its first copy, so its wait runs out: the kernel must record the timeout,
+exit (the prologue after freeing its tensor memory), and leave the context
 usable; gdn_device_status reports it once and then clears it."""
 import pytest
 import torch
@@ -14,13 +15,14 @@ from helpers import Runner
 pytestmark = pytest.mark.gpu
 
 
-def test_wait_timeout_is_reported_and_context_survives(cuda_device):
+@pytest.mark.parametrize("which", [1, 2], ids=["state_kernel", "prologue"])
+def test_wait_timeout_is_reported_and_context_survives(cuda_device, which):
     shape = wl.Shape(2, 2, 128, 128, 64, wl.BF16)
     w = wl.Workload("timeout", shape, seed=41, session_lengths=[256])
     run = Runner(shape, w.session_tokens(0), w.conv_weights(), cuda_device)
     assert gdn.gdn_device_status() == gdn.GDN_OK
     victim, out = run.session(), run.new_out()
-    gdn.gdn_debug_inject_wait_timeout(True, 2000)
+    gdn.gdn_debug_inject_wait_timeout(which, 2000)
     try:
         run.prefill(victim, 0, 256, out)
         status = gdn.gdn_device_status()
