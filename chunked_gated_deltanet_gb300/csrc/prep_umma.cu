@@ -50,15 +50,14 @@ constexpr uint32_t OFF_PH = OFF_BL + B_BYTES, OFF_PL = OFF_PH + R64_BYTES;     /
 constexpr uint32_t OFF_TBH = OFF_PL + R64_BYTES, OFF_TBL = OFF_TBH + R64_BYTES; // T, MN-major (B of P T)
 constexpr uint32_t OFF_AF = OFF_TBL + R64_BYTES;             // fp32 A (input of the inverse)
 constexpr uint32_t OFF_TF = OFF_AF + 4 * kBlock * LT;        // fp32 T
-constexpr uint32_t OFF_MT = OFF_TF + 4 * kBlock * LT;        // 3 x 16 x 17 inverse scratch
+constexpr uint32_t OFF_MT = OFF_TF + 4 * kBlock * LT;        // 2 x 16 x 24 inverse scratch
 constexpr uint32_t OFF_ATH = OFF_AF, OFF_ATL = OFF_ATH + 2 * R64_BYTES;   // [T; P T], K-major, over A and T
-constexpr uint32_t OFF_SMALL = OFF_MT + 4 * 3 * 16 * 17;     // gamma, beta, e^gamma
+constexpr uint32_t OFF_SMALL = OFF_MT + 4 * 2 * 16 * 24;     // gamma, beta, e^gamma
 constexpr uint32_t W_BYTES = D * 4 * 2;                      // conv weights of one head's channels (bf16 [D][4])
 constexpr uint32_t OFF_W = OFF_SMALL + 4 * 3 * kBlock;       // q, k, v conv weights
 constexpr uint32_t OFF_BAR = OFF_W + 3 * W_BYTES;            // [0] input copies, [1] MMA groups; TMEM slot
 constexpr uint32_t SMEM = OFF_BAR + 32;
 constexpr uint32_t RAW_ROW = 2 * D, RAW_TILE = (kBlock + 3) * RAW_ROW;
-constexpr uint32_t TILE_TX = RAW_TILE + W_BYTES;               // bytes one staged tile brings in
 constexpr uint32_t OFF_RAW = OFF_PH;                         // raw input tiles: dead before P, T, A are written
 static_assert(OFF_RAW + 3 * RAW_TILE <= OFF_SMALL, "raw tiles must fit the P, T and inverse regions");
 static_assert(OFF_ATL + 2 * R64_BYTES <= OFF_MT, "[T; P T] must fit over A and T");
@@ -115,6 +114,31 @@ __device__ __forceinline__ void put_cfrag16(float *base, int i, int c0, const fl
         float4 *dst = reinterpret_cast<float4 *>(base) + ((((c0 >> 4) * 4 + (i >> 4)) * 2 + h) * 32 + L);
         st_v8(dst, f0, f1);
     }
+}
+
+// c += X Y for a 16 x K block of X (row-major, pitch lx) and a K x 8 block of Y (row-major, pitch ly),
+// m16n8k8 tf32 MMAs with split operands (hi*hi + hi*lo + lo*hi: close to fp32 products); one warp.
+__device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, int lx, const float *Y, int ly, int K,
+                                               int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(X[g * lx + k0 + t], ah[0], al[0]);
+        split_tf32(X[(g + 8) * lx + k0 + t], ah[1], al[1]);
+        split_tf32(X[g * lx + k0 + t + 4], ah[2], al[2]);
+        split_tf32(X[(g + 8) * lx + k0 + t + 4], ah[3], al[3]);
+        split_tf32(Y[(k0 + t) * ly + g], bh[0], bl[0]);
+        split_tf32(Y[(k0 + t + 4) * ly + g], bh[1], bl[1]);
+        mma_tf32(c, al, bh);
+        mma_tf32(c, ah, bl);
+        mma_tf32(c, ah, bh);
+    }
+}
+// the m16n8 C fragment c (times s) into a row-major block Z (pitch lz)
+__device__ __forceinline__ void store_c16x8(float *Z, int lz, const float (&c)[4], float s, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2 *>(Z + g * lz + 2 * t) = make_float2(s * c[0], s * c[1]);
+    *reinterpret_cast<float2 *>(Z + (g + 8) * lz + 2 * t) = make_float2(s * c[2], s * c[3]);
 }
 
 // 8 fp32 values -> bf16 hi and lo halves, packed for one 16-byte core-matrix row each
@@ -185,28 +209,39 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     uint32_t in_phase = 0, mma_phase = 0;
     int in_pending = 0, mma_pending = 0;   // an issued copy group / MMA group not yet seen complete (CTA-uniform)
 
-    // Stage rows pos0-3 .. pos0+63 of `ntile` head tiles: one tensor copy of the block's 64 rows (rows past
-    // the inputs read as zero, rows past n belong to other tokens and only reach masked results) and three
-    // halo rows, from the inputs or, before a call's first token, from the conv state.
+    // Stage rows pos0-3 .. pos0+63 of `ntile` head tiles and their conv weights: one tensor copy of the
+    // block's 64 rows per tile (rows past the inputs read as zero, rows past n belong to other tokens and
+    // only reach masked results); the three halo rows (from the inputs or, before a call's first token,
+    // from the conv state) and the weights by plain 16-byte loads of warps 1-15.
     struct Tile { __nv_bfloat16 *dst, *wdst; const CUtensorMap *map; const __nv_bfloat16 *x; int64_t ld, col0, chan0; };
     auto stage = [&](const Tile *tl, int ntile, bool skip) {
-        if (warp == 0 && !skip) {
-            if (lane == 0) mbar_arrive_expect_tx(&bar[0], (uint32_t)ntile * TILE_TX);
+        in_pending = 1;
+        if (skip) return;
+        constexpr int HALO = 3 * (D / 8), WCH = W_BYTES / 16, PER = HALO + WCH;   // 16-byte chunks per tile
+        if (warp == 0) {
+            if (lane == 0) mbar_arrive_expect_tx(&bar[0], (uint32_t)ntile * kBlock * RAW_ROW);
             __syncwarp();
 #pragma unroll
+            for (int q = 0; q < 3; ++q)
+                if (q < ntile && lane == q) tma_load_2d(tl[q].dst + 3 * D, tl[q].map, (int)tl[q].col0, (int)row0, &bar[0]);
+        } else {
+            const int e = t - 32;
+#pragma unroll
             for (int q = 0; q < 3; ++q) {
-                if (q >= ntile) break;
-                if (lane == 30) tma_load_2d(tl[q].dst + 3 * D, tl[q].map, (int)tl[q].col0, (int)row0, &bar[0]);
-                if (lane == 31) bulk_g2s(tl[q].wdst, cw + tl[q].chan0 * 4, W_BYTES, &bar[0]);
-                if (lane >= 3 * q && lane < 3 * q + 3) {
-                    const int r = lane - 3 * q, pos = pos0 - 3 + r;
+                if (q >= ntile || e < PER * q || e >= PER * (q + 1)) continue;
+                const int k = e - PER * q;
+                if (k < HALO) {
+                    const int r = k / (D / 8), c = (k % (D / 8)) * 8, pos = pos0 - 3 + r;
                     const __nv_bfloat16 *src =
                         pos < 0 ? cs + (int64_t)(3 + pos) * ch + tl[q].chan0 : tl[q].x + (s.row0 + pos) * tl[q].ld + tl[q].col0;
-                    bulk_g2s(tl[q].dst + r * D, src, RAW_ROW, &bar[0]);
+                    *reinterpret_cast<uint4 *>(tl[q].dst + r * D + c) = __ldg(reinterpret_cast<const uint4 *>(src + c));
+                } else {
+                    const int kw = k - HALO;
+                    *reinterpret_cast<uint4 *>(tl[q].wdst + kw * 8) =
+                        __ldg(reinterpret_cast<const uint4 *>(cw + tl[q].chan0 * 4 + kw * 8));
                 }
             }
         }
-        in_pending = 1;
     };
     // every thread waits; true when the phase completed for all of them (CTA-uniform)
     auto wait_in = [&]() {
@@ -402,20 +437,30 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
         // 6. from TMEM: P (rows 0..63 -> bf16 hi/lo K-major) and A (rows 64..127 -> fp32)
         {
             const int q = warp & 3, cp = warp >> 2, R = 32 * q + lane, j0 = 16 * cp;
+            uint32_t r[16];
+            tmem_ld16_nowait(tmem + ((uint32_t)(32 * q) << 16) + j0, r);
+            float dec[16];   // e^{gamma_i - gamma_j}, while the load is in flight
+            {
+                const float gr = gam[R < kBlock ? R : R - kBlock];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) dec[jj] = __expf(gr - gam[j0 + jj]);
+            }
+            tmem_wait_ld(r);
             float v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + j0, v);
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(r[jj]);
             if (R < kBlock) {
                 const int i = R;
                 float pv[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) pv[jj] = (j0 + jj) <= i ? v[jj] * __expf(gam[i] - gam[j0 + jj]) : 0.f;
+                for (int jj = 0; jj < 16; ++jj) pv[jj] = (j0 + jj) <= i ? v[jj] * dec[jj] : 0.f;
                 store8(Ph, Pl, kmajor_bf16_offset(i, j0, K64_LBO, K64_SBO), pv);
                 store8(Ph, Pl, kmajor_bf16_offset(i, j0 + 8, K64_LBO, K64_SBO), pv + 8);
             } else {
                 const int i = R - kBlock;
                 float av[16];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) av[jj] = (j0 + jj) < i ? bet[i] * __expf(gam[i] - gam[j0 + jj]) * v[jj] : 0.f;
+                for (int jj = 0; jj < 16; ++jj) av[jj] = (j0 + jj) < i ? bet[i] * dec[jj] * v[jj] : 0.f;
 #pragma unroll
                 for (int c = 0; c < 16; c += 4)
                     *reinterpret_cast<float4 *>(Af + i * LT + j0 + c) = make_float4(av[c], av[c + 1], av[c + 2], av[c + 3]);
@@ -424,7 +469,10 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // 7. T = (I + A)^{-1} in fp32: diagonal 16x16 blocks by substitution, one column per thread
+        // 7. T = (I + A)^{-1} (unit lower triangular) in fp32, two levels of 2x2 blocking:
+        //    diagonal 16x16 blocks D_b by substitution (one column per thread; the other threads zero the
+        //    blocks above the diagonal), then T_10 = -D_1 A_10 D_0 and T_32 = -D_3 A_32 D_2, then
+        //    T[32:64, 0:32] = -T[32:64, 32:64] A[32:64, 0:32] T[0:32, 0:32]; products as split-tf32 MMAs
         if (t < kBlock) {
             const int d = t >> 4, c = t & 15;
             const float *Ad = Af + 16 * d * LT + 16 * d;
@@ -439,40 +487,52 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tf[(16 * d + i) * LT + 16 * d + c] = x[i];
+        } else {
+            for (int e = t - kBlock; e < 6 * 64; e += kUmmaPrepThreads - kBlock) {   // 6 blocks x 16 rows x 4 float4
+                const int bi = e >> 6, r = (e >> 2) & 15, c4 = e & 3;
+                const int ib = bi < 3 ? 0 : (bi < 5 ? 1 : 2), jb = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+                *reinterpret_cast<float4 *>(Tf + (16 * ib + r) * LT + 16 * jb + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         __syncthreads();
-        //    off-diagonal blocks by distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
-        for (int dist = 1; dist < 4; ++dist) {
-            const int nblkd = 4 - dist;
-            for (int e = t; e < nblkd * 256; e += kUmmaPrepThreads) {
-                const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15, ib = jb + dist;
-                float sum = 0.f;
-                for (int k = 16 * jb; k < 16 * ib; ++k) sum = fmaf(Af[(16 * ib + r) * LT + k], Tf[k * LT + 16 * jb + c], sum);
-                Mt[(jb * 16 + r) * 17 + c] = sum;
-            }
-            __syncthreads();
-            for (int e = t; e < nblkd * 256; e += kUmmaPrepThreads) {
-                const int jb = e >> 8, r = (e >> 4) & 15, c = e & 15, ib = jb + dist;
-                float sum = 0.f;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) sum = fmaf(Tf[(16 * ib + r) * LT + 16 * ib + k], Mt[(jb * 16 + k) * 17 + c], sum);
-                Tf[(16 * ib + r) * LT + 16 * jb + c] = -sum;
-            }
-            __syncthreads();
+        constexpr int LM = 24, LX = 40;
+        float *Xs = reinterpret_cast<float *>(TBh);   // 32 x LX scratch (the T operand regions are written later)
+        if (warp < 4) {   // warps 0,1: block pair (1, 0); warps 2,3: (3, 2); 8 columns each
+            const int b = 2 * (warp >> 1), nt = warp & 1;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3_tf32_16x8(c, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, 16, lane);
+            store_c16x8(Mt + (warp >> 1) * 16 * LM + 8 * nt, LM, c, 1.f, lane);
         }
+        __syncthreads();
+        if (warp < 4) {
+            const int b = 2 * (warp >> 1), nt = warp & 1;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3_tf32_16x8(c, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, Mt + (warp >> 1) * 16 * LM + 8 * nt, LM, 16, lane);
+            store_c16x8(Tf + 16 * (b + 1) * LT + 16 * b + 8 * nt, LT, c, -1.f, lane);
+        }
+        __syncthreads();
+        if (warp < 8) {   // X = A[32:64, 0:32] T[0:32, 0:32]: 2 m-tiles x 4 n-tiles
+            const int mt = warp >> 2, nt = warp & 3;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3_tf32_16x8(c, Af + (32 + 16 * mt) * LT, LT, Tf + 8 * nt, LT, 32, lane);
+            store_c16x8(Xs + 16 * mt * LX + 8 * nt, LX, c, 1.f, lane);
+        }
+        __syncthreads();
+        if (warp < 8) {   // T[32:64, 0:32] = -T[32:64, 32:64] X
+            const int mt = warp >> 2, nt = warp & 3;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3_tf32_16x8(c, Tf + (32 + 16 * mt) * LT + 32, LT, Xs + 8 * nt, LX, 32, lane);
+            store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, c, -1.f, lane);
+        }
+        __syncthreads();
         //    T as bf16 hi/lo: rows 0..63 of [T; P T] (K-major, written over A and T) and the B operand of
-        //    P T (MN-major); blocks above the diagonal are zero
+        //    P T (MN-major)
         {
             const int i = t & 63, kg = t >> 6;
             float v[8];
-            if ((kg >> 1) > (i >> 4)) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) v[c] = 0.f;
-            } else {
-                const float4 a = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg);
-                const float4 b = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg + 4);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-            }
+            const float4 a = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg);
+            const float4 b = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg + 4);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
             __syncthreads();   // every row of T is read before the first write over it
             store8(ATh, ATl, kmajor_bf16_offset(i, 8 * kg, K64_LBO, K64_SBO), v);
             store8(TBh, TBl, mnmajor_bf16_offset(8 * kg, i, K64_LBO, K64_SBO), v);
