@@ -212,6 +212,51 @@ class ReplayStep:
 
 
 # ---------------------------------------------------------------------------
+# Batched decode (one token for each of n sessions), captured once in a CUDA graph
+# ---------------------------------------------------------------------------
+
+def decode_measure(w, dev, n_sess: int = 64, steps: int = 50):
+    """Replays of one captured decode step over n_sess sessions of the bench layer; HBM roofline of the
+    step = every state read and written once, plus the conv states, inputs and outputs."""
+    import torch
+    from chunked_gated_deltanet_gb300 import gdn
+    sh = w.shape
+    desc = gdn.make_desc(sh.n_qk_heads, sh.n_v_heads, sh.d_k, sh.d_v, sh.grid_c, gdn.GDN_BF16, gdn.GDN_FP32)
+    sessions = [gdn.Session(desc, dev) for _ in range(n_sess)]
+    gen = torch.Generator(device=dev).manual_seed(5)
+    bf = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)
+    nq, nv = sh.n_qk_heads * sh.d_k, sh.n_v_heads * sh.d_v
+    xq, xk, xv = bf(n_sess, nq), bf(n_sess, nq), bf(n_sess, nv)
+    g = -0.1 * torch.nn.functional.softplus(torch.randn(n_sess, sh.n_v_heads, generator=gen, device=dev))
+    beta = torch.sigmoid(torch.randn(n_sess, sh.n_v_heads, generator=gen, device=dev))
+    cw = bf(2 * nq + nv, 4)
+    out = torch.empty((n_sess, sh.n_v_heads, sh.d_v), device=dev)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gdn.gdn_decode_step(desc, sessions, xq, xk, xv, g, beta, cw, out)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    state = n_sess * sh.n_v_heads * sh.d_k * sh.d_v * 4
+    conv = n_sess * 3 * (2 * nq + nv) * 2
+    io = n_sess * ((2 * nq + nv) * 2 + sh.n_v_heads * 8 + sh.n_v_heads * sh.d_v * 4)
+    bytes_step = 2 * state + 2 * conv + io
+    peak, _ = measured_peaks()
+    gbs = bytes_step / (us / 1e6) / 1e9
+    return {"sessions": n_sess, "launch": "CUDA graph replay of one gdn_decode_step", "us_per_step": round(us, 2),
+            "tokens_per_s": round(n_sess / (us / 1e6), 1), "bytes_per_step": bytes_step,
+            "achieved_gbs": round(gbs, 1), "peak_gbs": peak, "frac": round(gbs / peak, 4), "bound": "hbm"}
+
+
+# ---------------------------------------------------------------------------
 # CPU baseline: the oracle over a bounded sample
 # ---------------------------------------------------------------------------
 
@@ -281,6 +326,7 @@ def main():
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=41472)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -310,7 +356,6 @@ def main():
     clk.start()
     barrier()
     torch.cuda.synchronize()
-    gdn.gdn_timing_begin(100_000)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clk.mark("t0")
     ev0.record(stream)
@@ -321,6 +366,12 @@ def main():
     clk.mark("t1")
     barrier()
     ms = ev0.elapsed_time(ev1)
+    # --- the same steps again with an event pair around every launch (per-kernel times; kept out of the
+    #     region above, whose step time the extra event records would lengthen) ---
+    gdn.gdn_timing_begin(100_000)
+    for _ in range(args.steps):
+        step.step()
+    torch.cuda.synchronize()
     ktimes = gdn.gdn_timing_end()
     clocks = clk.stop()
     ms_max, tokens_all = reduce_max_sum(ms, step.tokens_per_step * args.steps)
@@ -366,10 +417,13 @@ def main():
                    "share": round(v[2] / sum(x[2] for x in ktimes.values()), 4)} for k, v in ktimes.items()}
     gpu_launches = int(sum(v[0] for v in ktimes.values()))
 
+    decode = None if args.no_decode else [decode_measure(w, dev, n) for n in (1, 64)]
+
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": step.config(),
-            "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline, "kernels": kernels, "clocks": clocks}
+            "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline, "kernels": kernels, "clocks": clocks,
+            "decode": decode}
 
     # --- CPU baseline (oracle), rank 0 at N=1 only ---
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -40,14 +40,34 @@ __global__ void __launch_bounds__(256) copy2_kernel(uint4 *d0, const uint4 *s0, 
     }
 }
 
-// One token of one session and v-head; thread j owns column j of S^T.
+// Sum over the 32 lanes of a warp of 16 per-lane values, scattered: afterwards
+// lanes 2c and 2c + 1 both hold the warp's total of value c (16 shuffles in all).
+__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16, half = 8; o >= 2; o >>= 1, half >>= 1) {
+        const bool up = lane & o;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+// One token of one session: CTA (session, 16-column slice of d_v) x v-head, thread i owns row i of the
+// slice of S^T (d_k x 16, in registers).
 //   u = beta (v - alpha S k),  S^T <- alpha S^T + k u^T,  o = S q
-// (the gated delta rule step with alpha = exp(g)).
+// (the gated delta rule step with alpha = exp(g)); the conv state is committed by conv_commit_kernel.
 template <int D, typename InT>
 __global__ void __launch_bounds__(D) decode_kernel(const LaunchCommon p, int64_t ch) {
-    __shared__ float qs[D], ks[D], red[2][D / 32];
-    const SessRef s = p.s[blockIdx.x];
-    const int h = blockIdx.y, hk = h / p.G, t = threadIdx.x;
+    constexpr int SC = 16, NW = D / 32, NSL = D / SC;
+    __shared__ float red[2][NW], part[NW][SC], vsh[SC], ush[SC];
+    const int si = blockIdx.x / NSL, sl = blockIdx.x % NSL, c0 = sl * SC;
+    const SessRef s = p.s[si];
+    const int h = blockIdx.y, hk = h / p.G, t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int64_t nq = (int64_t)p.Hk * D, nv = (int64_t)p.Hv * D;
     const InT *cw = static_cast<const InT *>(p.conv_w);
     const InT *cs = static_cast<const InT *>(s.conv);
@@ -58,38 +78,65 @@ __global__ void __launch_bounds__(D) decode_kernel(const LaunchCommon p, int64_t
         const float x0 = to_f(static_cast<const InT *>(xp)[s.row0 * ld + col]);
         return conv_tap<InT>(w, to_f(cs[chan]), to_f(cs[ch + chan]), to_f(cs[2 * ch + chan]), x0, p.act);
     };
+    // the slice of S^T: row t, columns c0 .. c0 + 15
+    float *Srow = s.S + (int64_t)h * D * D + (int64_t)t * D + c0;
+    float st[SC];
+#pragma unroll
+    for (int c = 0; c < SC; c += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(Srow + c);
+        st[c] = v.x; st[c + 1] = v.y; st[c + 2] = v.z; st[c + 3] = v.w;
+    }
     const float yq = conv1(p.xq, nq, (int64_t)hk * D + t, (int64_t)hk * D + t);
     const float yk = conv1(p.xk, nq, (int64_t)hk * D + t, nq + (int64_t)hk * D + t);
-    const float yv = conv1(p.xv, nv, (int64_t)h * D + t, 2 * nq + (int64_t)h * D + t);
+    if (t < SC) vsh[t] = conv1(p.xv, nv, (int64_t)h * D + c0 + t, 2 * nq + (int64_t)h * D + c0 + t);
     float sq = yq * yq, sk = yk * yk;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         sq += __shfl_xor_sync(0xffffffffu, sq, o);
         sk += __shfl_xor_sync(0xffffffffu, sk, o);
     }
-    if ((t & 31) == 0) { red[0][t >> 5] = sq; red[1][t >> 5] = sk; }
+    if (lane == 0) { red[0][warp] = sq; red[1][warp] = sk; }
     __syncthreads();
     float tq = 0.f, tk = 0.f;
 #pragma unroll
-    for (int w = 0; w < D / 32; ++w) { tq += red[0][w]; tk += red[1][w]; }
-    qs[t] = yq * (p.q_scale / sqrtf(tq + p.eps));
-    ks[t] = yk * (1.f / sqrtf(tk + p.eps));
-    __syncthreads();
-
-    float *S = s.S + (int64_t)h * D * D;
+    for (int w = 0; w < NW; ++w) { tq += red[0][w]; tk += red[1][w]; }
+    const float qt = yq * (p.q_scale / sqrtf(tq + p.eps));
+    const float kt = yk * (1.f / sqrtf(tk + p.eps));
     const float alpha = expf(p.g[s.row0 * p.Hv + h]), b = p.beta[s.row0 * p.Hv + h];
-    float kS = 0.f;
-    for (int i = 0; i < D; ++i) kS = fmaf(ks[i], S[i * D + t], kS);
-    const float u = b * (yv - alpha * kS);
-    float o = 0.f;
-    for (int i = 0; i < D; ++i) {
-        const float sn = fmaf(ks[i], u, alpha * S[i * D + t]);
-        S[i * D + t] = sn;
-        o = fmaf(sn, qs[i], o);
+
+    // (S k)_j over the slice's columns: column sums of k_t S[t][j]
+    float v[SC];
+#pragma unroll
+    for (int c = 0; c < SC; ++c) v[c] = kt * st[c];
+    float r = warp_reduce_scatter16(v);
+    if (!(lane & 1)) part[warp][lane >> 1] = r;
+    __syncthreads();
+    if (t < SC) {
+        float kS = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) kS += part[w][t];
+        ush[t] = b * (vsh[t] - alpha * kS);
     }
-    const int64_t oi = (s.row0 * p.Hv + h) * D + t;
-    if (p.out_bf16) static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(o);
-    else static_cast<float *>(p.out)[oi] = o;
+    __syncthreads();
+    // S^T <- alpha S^T + k u^T, written back; o_j = (S q)_j
+#pragma unroll
+    for (int c = 0; c < SC; ++c) {
+        st[c] = fmaf(kt, ush[c], alpha * st[c]);
+        v[c] = st[c] * qt;
+    }
+#pragma unroll
+    for (int c = 0; c < SC; c += 4) *reinterpret_cast<float4 *>(Srow + c) = make_float4(st[c], st[c + 1], st[c + 2], st[c + 3]);
+    r = warp_reduce_scatter16(v);
+    if (!(lane & 1)) part[warp][lane >> 1] = r;   // the (S k) partials were consumed before the barrier above
+    __syncthreads();
+    if (t < SC) {
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) o += part[w][t];
+        const int64_t oi = (s.row0 * p.Hv + h) * D + c0 + t;
+        if (p.out_bf16) static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(o);
+        else static_cast<float *>(p.out)[oi] = o;
+    }
 }
 
 }  // namespace gdn
@@ -116,7 +163,7 @@ cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *d
 
 cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st) {
     using namespace gdn;
-    dim3 grid(p.n_sess, p.Hv);
+    dim3 grid(p.n_sess * (D / 16), p.Hv);
     if (D == 64) {
         if (in_bf16) decode_kernel<64, __nv_bfloat16><<<grid, 64, 0, st>>>(p, ch);
         else decode_kernel<64, float><<<grid, 64, 0, st>>>(p, ch);

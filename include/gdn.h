@@ -190,7 +190,14 @@ gdn_status gdn_conv_state(const gdn_layer_desc *desc, const gdn_session *session
 
 /* One token for each of n_sessions sessions (a decode step; leaves sessions
  * off grid). Row i of xq, xk ([n][Hk*d_k]), xv ([n][Hv*d_v]), g, beta ([n][Hv])
- * and out ([n][Hv][d_v]) belongs to sessions[i]; committed grows by one. */
+ * and out ([n][Hv][d_v]) belongs to sessions[i]; committed grows by one.
+ * Defined by the gated delta rule for one token (the recurrence of "Gated
+ * Delta Networks", section 3, with the layer's conv and L2 norm). The call
+ * allocates nothing and never waits on the host, and its kernels reach the
+ * states only through the sessions' device addresses: it can be captured in
+ * a CUDA graph on `stream` and replayed with new inputs copied into the same
+ * buffers. A replay advances the device states only; `committed` counts the
+ * host calls. Errors as for the prefill calls; nothing is launched on error. */
 gdn_status gdn_decode_step(const gdn_layer_desc *desc, gdn_session *sessions, int32_t n_sessions,
                            const void *xq, const void *xk, const void *xv, const float *g,
                            const float *beta, const void *conv_w, void *out, gdn_stream_t stream);
