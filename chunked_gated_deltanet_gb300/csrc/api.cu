@@ -2,6 +2,7 @@
 // host before any device work, workspace layout, and launch orchestration.
 #include "gdn.h"
 #include "common.cuh"
+#include "host.h"
 
 #include <cudaTypedefs.h>
 
@@ -17,7 +18,7 @@
 using gdn::kBlock;
 using gdn::LaunchCommon;
 
-namespace {
+namespace gdn_host {
 
 thread_local char g_err[512] = "";
 
@@ -87,6 +88,12 @@ gdn_status check_state(const gdn_layer_desc *d, const gdn_session *s, const char
         return fail(GDN_ERR_STATE_MISMATCH, "%s is a missing slot (committed = %lld)", what, (long long)s->committed);
     return GDN_OK;
 }
+
+}  // namespace gdn_host
+
+using namespace gdn_host;
+
+namespace {
 
 // Workspace layout for a launch of up to nblk blocks. Offsets count from the workspace pointer
 // rounded up to 256 bytes (the kernels' widest stores want 32-byte alignment); `bytes` includes
@@ -530,6 +537,8 @@ GDN_API const char *gdn_status_string(gdn_status s) {
         case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
         case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+        case GDN_ERR_NOT_FOUND: return "GDN_ERR_NOT_FOUND";
+        case GDN_ERR_IO: return "GDN_ERR_IO";
     }
     return "unknown status";
 }

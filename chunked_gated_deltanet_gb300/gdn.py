@@ -23,6 +23,8 @@ GDN_ERR_STATE_MISMATCH = 4
 GDN_ERR_WORKSPACE = 5
 GDN_ERR_CUDA = 6
 GDN_ERR_TIMEOUT = 7
+GDN_ERR_NOT_FOUND = 8
+GDN_ERR_IO = 9
 GDN_FP32 = 0
 GDN_BF16 = 1
 GDN_CONV_NONE = 0
@@ -34,7 +36,8 @@ EXPORTED = ["gdn_desc_tag", "gdn_desc_check", "gdn_state_bytes", "gdn_conv_state
             "gdn_workspace_size", "gdn_prefill_chunks", "gdn_prefill_varlen", "gdn_state_capture",
             "gdn_state_restore", "gdn_conv_state", "gdn_decode_step", "gdn_timing_begin", "gdn_timing_end",
             "gdn_prefill_chunks_noalloc", "gdn_device_status", "gdn_debug_inject_wait_timeout",
-            "gdn_last_error", "gdn_status_string"]
+            "gdn_last_error", "gdn_status_string", "gdn_state_blob_bytes", "gdn_state_serialize",
+            "gdn_state_deserialize", "gdn_state_save", "gdn_state_load"]
 
 
 class gdn_layer_desc(ctypes.Structure):
@@ -98,6 +101,11 @@ def load_library(path: Optional[str] = None):
         "gdn_debug_inject_wait_timeout": (ctypes.c_int, [i32, i64]),
         "gdn_last_error": (ctypes.c_char_p, []),
         "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "gdn_state_blob_bytes": (ctypes.c_size_t, [D]),
+        "gdn_state_serialize": (ctypes.c_int, [D, Sp, vp, ctypes.c_size_t, vp]),
+        "gdn_state_deserialize": (ctypes.c_int, [D, vp, ctypes.c_size_t, Sp, vp]),
+        "gdn_state_save": (ctypes.c_int, [D, Sp, ctypes.c_char_p, vp]),
+        "gdn_state_load": (ctypes.c_int, [D, ctypes.c_char_p, Sp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -262,6 +270,33 @@ def gdn_decode_step(desc, sessions: Sequence[Session], xq, xk, xv, g, beta, conv
     for i, s in enumerate(sessions):
         s.c.committed = arr[i].committed
     _check(st)
+
+
+def gdn_state_blob_bytes(desc) -> int:
+    return int(load_library().gdn_state_blob_bytes(ctypes.byref(desc)))
+
+
+def gdn_state_serialize(desc, session: Session, blob: torch.Tensor, stream=None):
+    """Serialise into `blob` (a uint8 host tensor, pinned for an asynchronous copy)."""
+    _check(load_library().gdn_state_serialize(ctypes.byref(desc), ctypes.byref(session.c), _ptr(blob),
+                                              blob.numel() * blob.element_size(), _stream(stream)))
+
+
+def gdn_state_deserialize(desc, blob: torch.Tensor, dst: Session, stream=None):
+    lib = load_library()
+    st = lib.gdn_state_deserialize(ctypes.byref(desc), _ptr(blob), blob.numel() * blob.element_size(),
+                                   ctypes.byref(dst.c), _stream(stream))
+    _check(st)
+
+
+def gdn_state_save(desc, session: Session, path: str, stream=None):
+    _check(load_library().gdn_state_save(ctypes.byref(desc), ctypes.byref(session.c), os.fsencode(path),
+                                         _stream(stream)))
+
+
+def gdn_state_load(desc, path: str, dst: Session, stream=None):
+    _check(load_library().gdn_state_load(ctypes.byref(desc), os.fsencode(path), ctypes.byref(dst.c),
+                                         _stream(stream)))
 
 
 def gdn_timing_begin(max_launches: int):

@@ -54,7 +54,9 @@ typedef enum gdn_status {
     GDN_ERR_STATE_MISMATCH = 4, /* session / slot belongs to another layer description, or slot is missing */
     GDN_ERR_WORKSPACE = 5,      /* workspace too small */
     GDN_ERR_CUDA = 6,           /* a CUDA call or launch failed */
-    GDN_ERR_TIMEOUT = 7         /* reserved for bounded device waits */
+    GDN_ERR_TIMEOUT = 7,        /* a bounded device wait ran out (see gdn_device_status) */
+    GDN_ERR_NOT_FOUND = 8,      /* no saved state at the given path */
+    GDN_ERR_IO = 9              /* a file could not be written or read */
 } gdn_status;
 
 enum { GDN_FP32 = 0, GDN_BF16 = 1 };
@@ -187,6 +189,50 @@ gdn_status gdn_state_restore(const gdn_layer_desc *desc, gdn_session *dst, const
  * `out`, which may be device memory or pinned host memory. */
 gdn_status gdn_conv_state(const gdn_layer_desc *desc, const gdn_session *session, void *out,
                           gdn_stream_t stream);
+
+/* ---- Serialised states (host memory and files) ----
+ *
+ * A blob is a 128-byte header followed by S (fp32 [Hv][d_k][d_v]) and the
+ * conv state (in_dtype [3][ch]), gdn_state_blob_bytes(desc) bytes in all.
+ * Header, little-endian: "GDNSTATE" (8 bytes), version 1 (u32), header bytes
+ * 128 (u32), layer tag (u64), n_qk_heads, n_v_heads, d_k, d_v, grid_c,
+ * in_dtype (6 x i32), committed (i64), S bytes (u64), conv bytes (u64),
+ * payload checksum (u64; 0 = not computed), completion marker (u64), zero
+ * padding. The completion marker is written last, after the payload is in
+ * place; a blob without it reads as missing, never as an older state.
+ * Restoring refuses a blob of another layer description (tag, shapes, grid),
+ * of another format version, a blob without its completion marker and one
+ * whose checksum does not match, with GDN_ERR_STATE_MISMATCH, and changes
+ * nothing then. */
+size_t gdn_state_blob_bytes(const gdn_layer_desc *desc);
+
+/* Serialises a session (or slot) into `blob` (host memory, pinned for an
+ * asynchronous copy, of blob_bytes >= gdn_state_blob_bytes). The header is
+ * written at once with the marker cleared; the payload copies and then the
+ * marker follow in `stream` order. The blob must stay allocated, and must not
+ * be read as complete, until the stream has passed the call. */
+gdn_status gdn_state_serialize(const gdn_layer_desc *desc, const gdn_session *session, void *blob,
+                               size_t blob_bytes, gdn_stream_t stream);
+
+/* Restores a blob into `dst` (its own device buffers): validates the header
+ * on the host, then enqueues the copies on `stream` and sets dst->committed
+ * and dst->tag. The blob must stay allocated until the stream has passed the
+ * copies. */
+gdn_status gdn_state_deserialize(const gdn_layer_desc *desc, const void *blob, size_t blob_bytes,
+                                 gdn_session *dst, gdn_stream_t stream);
+
+/* Saves a session to the file `path` with a payload checksum. Write
+ * protocol: the old file is removed first, the blob goes to "<path>.tmp",
+ * is flushed to disk and renamed over `path`, then the directory is flushed:
+ * after a failure at any point the path holds either the new state or
+ * nothing. Synchronises `stream`. GDN_ERR_IO on a file error. */
+gdn_status gdn_state_save(const gdn_layer_desc *desc, const gdn_session *session, const char *path,
+                          gdn_stream_t stream);
+
+/* Loads the file `path` into `dst` (validation as gdn_state_deserialize, and
+ * the checksum); synchronises `stream`. GDN_ERR_NOT_FOUND if there is no file,
+ * GDN_ERR_IO if it cannot be read. */
+gdn_status gdn_state_load(const gdn_layer_desc *desc, const char *path, gdn_session *dst, gdn_stream_t stream);
 
 /* One token for each of n_sessions sessions (a decode step; leaves sessions
  * off grid). Row i of xq, xk ([n][Hk*d_k]), xv ([n][Hv*d_v]), g, beta ([n][Hv])
