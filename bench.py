@@ -257,6 +257,59 @@ def decode_measure(w, dev, n_sess: int = 64, steps: int = 50):
 
 
 # ---------------------------------------------------------------------------
+# Branches of one shared prefix: one call reading the prefix state in place vs restore + prefill per branch
+# ---------------------------------------------------------------------------
+
+def branches_measure(dev, reps: int = 20):
+    import torch
+    from chunked_gated_deltanet_gb300 import gdn
+    from chunked_gated_deltanet_gb300 import workloads as wl
+    w = wl.shared_prefix()
+    sh = w.shape
+    desc = gdn.make_desc(sh.n_qk_heads, sh.n_v_heads, sh.d_k, sh.d_v, sh.grid_c, gdn.GDN_BF16, gdn.GDN_FP32)
+    cut = wl.grid_floor(w.request_prefix, sh.grid_c)
+    x_req = wl.tokens_to_torch(w.session_tokens(0, cut), sh.dtype, dev)
+    cw = wl.to_torch(w.conv_weights(), sh.dtype, dev)
+    lengths = [n for br in w.branches for n in br]
+    tails = [w.extra_tokens(200 + i, n) for i, n in enumerate(lengths)]
+    cu = [0]
+    for t in tails:
+        cu.append(cu[-1] + len(t))
+    x = wl.tokens_to_torch(wl.Tokens.concat(tails), sh.dtype, dev)
+    out = torch.empty((cu[-1], sh.n_v_heads, sh.d_v), device=dev)
+    ws = gdn.workspace(desc, cu[-1] + 64 * len(tails) + cut, len(tails), dev)
+    prefix = gdn.Session(desc, dev)
+    gdn.gdn_prefill_chunks(desc, prefix, *x_req, cw, torch.empty((cut, sh.n_v_heads, sh.d_v), device=dev), ws)
+    branches = [gdn.Session(desc, dev) for _ in tails]
+
+    def per_branch():
+        for i, b in enumerate(branches):
+            gdn.gdn_state_restore(desc, b, prefix)
+            a, e = cu[i], cu[i + 1]
+            gdn.gdn_prefill_chunks(desc, b, *(t[a:e] for t in x), cw, out[a:e], ws, flags=gdn.GDN_ALLOW_PARTIAL)
+
+    def one_call():
+        gdn.gdn_prefill_branches(desc, prefix, branches, cu, *x, cw, out, ws, flags=gdn.GDN_ALLOW_PARTIAL)
+
+    res = {}
+    for name, fn in (("restore_and_prefill_per_branch", per_branch), ("one_branches_call", one_call)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = round(e0.elapsed_time(e1) * 1e3 / reps, 1)
+    return {"workload": f"{len(tails)} branches of {min(lengths)}-{max(lengths)} tokens ({cu[-1]} in all) from a "
+                        f"{cut}-token prefix state, {sh.n_v_heads} heads, d={sh.d_k}, grid {sh.grid_c}",
+            "us_per_round": res, "tokens_per_s_one_call": round(cu[-1] / (res["one_branches_call"] / 1e6), 1),
+            "speedup": round(res["restore_and_prefill_per_branch"] / res["one_branches_call"], 2)}
+
+
+# ---------------------------------------------------------------------------
 # CPU baseline: the oracle over a bounded sample
 # ---------------------------------------------------------------------------
 
@@ -326,7 +379,7 @@ def main():
     ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode and branch measurements")
     ap.add_argument("--cpu-sample-tokens", type=int, default=41472)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -418,12 +471,13 @@ def main():
     gpu_launches = int(sum(v[0] for v in ktimes.values()))
 
     decode = None if args.no_decode else [decode_measure(w, dev, n) for n in (1, 64)]
+    branches = None if args.no_decode else branches_measure(dev)
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": step.config(),
             "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline, "kernels": kernels, "clocks": clocks,
-            "decode": decode}
+            "decode": decode, "branches": branches}
 
     # --- CPU baseline (oracle), rank 0 at N=1 only ---
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

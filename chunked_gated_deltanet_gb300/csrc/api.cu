@@ -284,13 +284,17 @@ GDN_API size_t gdn_workspace_size(const gdn_layer_desc *d, int64_t max_tokens, i
     return ws_layout(d, nblk).bytes;
 }
 
-GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sessions, int32_t n_sessions,
-                                      const int64_t *cu, const void *xq, const void *xk, const void *xv,
-                                      const float *g, const float *beta, const void *conv_w, uint32_t flags,
-                                      void *out, int64_t *n_consumed, void *workspace, size_t workspace_bytes,
-                                      gdn_stream_t stream) {
+namespace {
+
+// Prefill of n sessions; with `prefix`, every session starts from the prefix's state (read in place) and
+// receives its own result, as if the prefix had been restored into it first.
+gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t n_sessions, const int64_t *cu,
+                        const void *xq, const void *xk, const void *xv, const float *g, const float *beta,
+                        const void *conv_w, uint32_t flags, void *out, int64_t *n_consumed, void *workspace,
+                        size_t workspace_bytes, gdn_stream_t stream, const gdn_session *prefix) {
     gdn_status st = check_desc(d);
     if (st != GDN_OK) return st;
+    if (prefix && (st = check_state(d, prefix, "prefix", true)) != GDN_OK) return st;
     if (flags & ~GDN_ALLOW_PARTIAL) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     if (n_sessions < 1 || n_sessions > GDN_MAX_SESSIONS)
         return fail(GDN_ERR_INVALID_ARG, "n_sessions must be in [1, %d] (got %d)", GDN_MAX_SESSIONS, n_sessions);
@@ -305,20 +309,23 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
         if (len < 0) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens must be non-decreasing (at %d)", i);
         if (len > (int64_t)1 << 30) return fail(GDN_ERR_INVALID_ARG, "session %d: more than 2^30 tokens in one call", i);
         char what[48];
-        snprintf(what, sizeof(what), "session %d", i);
-        if ((st = check_state(d, &sessions[i], what, true)) != GDN_OK) return st;
-        if (!partial && sessions[i].committed % C != 0)
-            return fail(GDN_ERR_OFF_GRID, "session %d is off grid (committed %lld, grid %d): only a partial call, "
-                        "a decode step or a restore may follow", i, (long long)sessions[i].committed, C);
+        snprintf(what, sizeof(what), prefix ? "branch %d" : "session %d", i);
+        if ((st = check_state(d, &sessions[i], what, !prefix)) != GDN_OK) return st;
+        const int64_t base = prefix ? prefix->committed : sessions[i].committed;
+        if (!partial && base % C != 0)
+            return fail(GDN_ERR_OFF_GRID, "%s is off grid (committed %lld, grid %d): only a partial call, "
+                        "a decode step or a restore may follow", prefix ? "the prefix" : what, (long long)base, C);
         nproc[i] = partial ? len : (len / C) * C;
         total += nproc[i];
     }
     {
         std::vector<const void *> ptrs(n_sessions);
         for (int i = 0; i < n_sessions; ++i) ptrs[i] = sessions[i].S;
+        if (prefix) ptrs.push_back(prefix->S);
         std::sort(ptrs.begin(), ptrs.end());
         if (std::adjacent_find(ptrs.begin(), ptrs.end()) != ptrs.end())
-            return fail(GDN_ERR_INVALID_ARG, "the sessions of one call must be distinct");
+            return fail(GDN_ERR_INVALID_ARG, prefix ? "the branches and the prefix must be distinct sessions"
+                                                    : "the sessions of one call must be distinct");
     }
     // blocks per launch batch, and the workspace that needs
     int64_t max_batch_blocks = 0;
@@ -369,6 +376,8 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
                 gdn::SessRef &r = p.s[cnt++];
                 r.row0 = cu[i]; r.n = (int32_t)nproc[i]; r.blk0 = blk;
                 r.S = sessions[i].S; r.conv = sessions[i].conv;
+                r.S0 = prefix ? prefix->S : r.S;
+                r.conv0 = prefix ? prefix->conv : r.conv;
                 blk += (int)((nproc[i] + kBlock - 1) / kBlock);
             }
             i0 = i;
@@ -392,11 +401,43 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
             if (e != cudaSuccess) return cuda_fail(e, "state/output kernel");
         }
     }
+    if (prefix) {   // a branch with nothing to process becomes a copy of the prefix
+        cudaStream_t cst = (cudaStream_t)stream;
+        for (int i = 0; i < n_sessions; ++i) {
+            if (nproc[i] > 0) continue;
+            cudaError_t e = launch_k(K_COPY, cst, [&] {
+                return gdn_launch_copy(sessions[i].S, prefix->S, gdn_state_bytes(d), sessions[i].conv, prefix->conv,
+                                       gdn_conv_state_bytes(d), cst);
+            });
+            if (e != cudaSuccess) return cuda_fail(e, "prefix copy");
+        }
+    }
     for (int i = 0; i < n_sessions; ++i) {
-        sessions[i].committed += nproc[i];
+        sessions[i].committed = (prefix ? prefix->committed : sessions[i].committed) + nproc[i];
         n_consumed[i] = nproc[i];
     }
     return GDN_OK;
+}
+
+}  // namespace
+
+GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sessions, int32_t n_sessions,
+                                      const int64_t *cu, const void *xq, const void *xk, const void *xv,
+                                      const float *g, const float *beta, const void *conv_w, uint32_t flags,
+                                      void *out, int64_t *n_consumed, void *workspace, size_t workspace_bytes,
+                                      gdn_stream_t stream) {
+    return prefill_impl(d, sessions, n_sessions, cu, xq, xk, xv, g, beta, conv_w, flags, out, n_consumed, workspace,
+                        workspace_bytes, stream, nullptr);
+}
+
+GDN_API gdn_status gdn_prefill_branches(const gdn_layer_desc *d, const gdn_session *prefix, gdn_session *branches,
+                                        int32_t n_branches, const int64_t *cu, const void *xq, const void *xk,
+                                        const void *xv, const float *g, const float *beta, const void *conv_w,
+                                        uint32_t flags, void *out, int64_t *n_consumed, void *workspace,
+                                        size_t workspace_bytes, gdn_stream_t stream) {
+    if (!prefix) return fail(GDN_ERR_INVALID_ARG, "prefix is NULL");
+    return prefill_impl(d, branches, n_branches, cu, xq, xk, xv, g, beta, conv_w, flags, out, n_consumed, workspace,
+                        workspace_bytes, stream, prefix);
 }
 
 GDN_API gdn_status gdn_prefill_chunks(const gdn_layer_desc *d, gdn_session *session, const void *xq,
@@ -492,6 +533,7 @@ GDN_API gdn_status gdn_decode_step(const gdn_layer_desc *d, gdn_session *session
             gdn::SessRef &r = p.s[j];
             r.row0 = i0 + j; r.n = 1; r.blk0 = 0;
             r.S = sessions[i0 + j].S; r.conv = sessions[i0 + j].conv;
+            r.S0 = r.S; r.conv0 = r.conv;
         }
         p.n_sess = cnt; p.nblk = 0;
         cudaStream_t cst = (cudaStream_t)stream;

@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
             else if (chan < 2 * nq) { x = static_cast<const __nv_bfloat16 *>(p.xk); col = chan - nq; ld = nq; }
             else { x = static_cast<const __nv_bfloat16 *>(p.xv); col = chan - 2 * nq; ld = nv; }
             __nv_bfloat16 *cs = static_cast<__nv_bfloat16 *>(s.conv);
-            const __nv_bfloat16 o0 = cs[chan], o1 = cs[ch + chan], o2 = cs[2 * ch + chan];
+            const __nv_bfloat16 *cs0 = static_cast<const __nv_bfloat16 *>(s.conv0);
+            const __nv_bfloat16 o0 = cs0[chan], o1 = cs0[ch + chan], o2 = cs0[2 * ch + chan];
             __nv_bfloat16 nw[3];
 #pragma unroll
             for (int r = 0; r < 3; ++r) {
@@ -90,15 +91,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
 
     // state rows in registers (fp32), tf32 copy in shared memory
     float *Sg = s.S + (int64_t)h * D * D;
+    const float *Sg0 = s.S0 + (int64_t)h * D * D;   // the starting state (the session's own, or a prefix's)
     float st[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int c = 8 * nt + 2 * t4;
         if (owner) {
-            st[nt][0] = Sg[(int64_t)m0 * D + c0 + c];
-            st[nt][1] = Sg[(int64_t)m0 * D + c0 + c + 1];
-            st[nt][2] = Sg[(int64_t)(m0 + 8) * D + c0 + c];
-            st[nt][3] = Sg[(int64_t)(m0 + 8) * D + c0 + c + 1];
+            st[nt][0] = Sg0[(int64_t)m0 * D + c0 + c];
+            st[nt][1] = Sg0[(int64_t)m0 * D + c0 + c + 1];
+            st[nt][2] = Sg0[(int64_t)(m0 + 8) * D + c0 + c];
+            st[nt][3] = Sg0[(int64_t)(m0 + 8) * D + c0 + c + 1];
             St[m0 * SP + c] = tf32_round(st[nt][0]);
             St[m0 * SP + c + 1] = tf32_round(st[nt][1]);
             St[(m0 + 8) * SP + c] = tf32_round(st[nt][2]);

@@ -17,8 +17,10 @@ struct SessRef {
     int64_t row0;    // first row of the session's tokens in the packed inputs / outputs
     int32_t n;       // tokens processed for this session in this call
     int32_t blk0;    // index of its first 64-token block in the launch's block numbering
-    float *S;        // fp32 [Hv][D][D] state (transposed)
-    void *conv;      // in_dtype [3][ch] conv state
+    float *S;        // fp32 [Hv][D][D] state (transposed): the result goes here
+    void *conv;      // in_dtype [3][ch] conv state: the result goes here
+    const float *S0;      // the state the call starts from (S itself, or a shared prefix's state)
+    const void *conv0;    // the conv state it starts from (conv itself, or the prefix's)
 };
 
 struct LaunchCommon {

@@ -19,12 +19,13 @@ __global__ void __launch_bounds__(256) conv_commit_kernel(const LaunchCommon p, 
     else if (chan < 2 * nq) { x = static_cast<const InT *>(p.xk); col = chan - nq; ld = nq; }
     else { x = static_cast<const InT *>(p.xv); col = chan - 2 * nq; ld = nv; }
     InT *cs = static_cast<InT *>(s.conv);
-    const InT old[3] = {cs[chan], cs[ch + chan], cs[2 * ch + chan]};
+    const InT *cs0 = static_cast<const InT *>(s.conv0);
+    const InT o0 = cs0[chan], o1 = cs0[ch + chan], o2 = cs0[2 * ch + chan];
     InT nw[3];
 #pragma unroll
     for (int r = 0; r < 3; ++r) {
         const int pos = s.n - 3 + r;
-        nw[r] = pos >= 0 ? x[(s.row0 + pos) * ld + col] : old[3 + pos];
+        nw[r] = pos >= 0 ? x[(s.row0 + pos) * ld + col] : (pos == -3 ? o0 : (pos == -2 ? o1 : o2));
     }
 #pragma unroll
     for (int r = 0; r < 3; ++r) cs[r * ch + chan] = nw[r];

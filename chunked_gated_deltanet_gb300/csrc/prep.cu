@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(const LaunchCommon p,
     const int Hk = p.Hk, Hv = p.Hv;
     const int64_t nq = (int64_t)Hk * D, nv = (int64_t)Hv * D;
     const InT *cw = static_cast<const InT *>(p.conv_w);
-    const InT *cs = static_cast<const InT *>(s.conv);
+    const InT *cs = static_cast<const InT *>(s.conv0);
 
     // 1. conv of the q and k channels of head hk (one channel per thread, sliding window)
     if (t < 2 * D) {

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prep_tc_kernel(const LaunchCo
     const int Hk = p.Hk, Hv = p.Hv;
     const int64_t nq = (int64_t)Hk * D, nv = (int64_t)Hv * D;
     const __nv_bfloat16 *cw = static_cast<const __nv_bfloat16 *>(p.conv_w);
-    const __nv_bfloat16 *cs = static_cast<const __nv_bfloat16 *>(s.conv);
+    const __nv_bfloat16 *cs = static_cast<const __nv_bfloat16 *>(s.conv0);
 
     // Stage rows pos0-3 .. pos0+63 of one head's channels; rows before the call
     // come from the conv state, rows past the block's valid rows are zero.

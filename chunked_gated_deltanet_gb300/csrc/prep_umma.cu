@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     const int Hk = p.Hk, Hv = p.Hv;
     const int64_t nq = (int64_t)Hk * D, nv = (int64_t)Hv * D;
     const __nv_bfloat16 *cw = static_cast<const __nv_bfloat16 *>(p.conv_w);
-    const __nv_bfloat16 *cs = static_cast<const __nv_bfloat16 *>(s.conv);
+    const __nv_bfloat16 *cs = static_cast<const __nv_bfloat16 *>(s.conv0);
 
     if (warp == 0) {
         tmem_alloc(tslot, 512);

@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const LaunchCommon p
     const int Hv = p.Hv;
 
     float *Sg = s.S + (int64_t)h * D * D;
-    for (int e = t; e < D * DS; e += kThreads) St[e] = Sg[(e / DS) * D + c0 + e % DS];
+    const float *Sg0 = s.S0 + (int64_t)h * D * D;   // the starting state (the session's own, or a prefix's)
+    for (int e = t; e < D * DS; e += kThreads) St[e] = Sg0[(e / DS) * D + c0 + e % DS];
 
     const int c = t % DS, i0 = t / DS;   // rows i0 + 16 r (outputs), key rows i0 + 16 r (state)
     const int nb = (s.n + kBlock - 1) / kBlock;

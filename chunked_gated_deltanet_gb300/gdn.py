@@ -37,7 +37,7 @@ EXPORTED = ["gdn_desc_tag", "gdn_desc_check", "gdn_state_bytes", "gdn_conv_state
             "gdn_state_restore", "gdn_conv_state", "gdn_decode_step", "gdn_timing_begin", "gdn_timing_end",
             "gdn_prefill_chunks_noalloc", "gdn_device_status", "gdn_debug_inject_wait_timeout",
             "gdn_last_error", "gdn_status_string", "gdn_state_blob_bytes", "gdn_state_serialize",
-            "gdn_state_deserialize", "gdn_state_save", "gdn_state_load"]
+            "gdn_state_deserialize", "gdn_state_save", "gdn_state_load", "gdn_prefill_branches"]
 
 
 class gdn_layer_desc(ctypes.Structure):
@@ -91,6 +91,8 @@ def load_library(path: Optional[str] = None):
         "gdn_prefill_varlen": (ctypes.c_int, [D, Sp, i32, I64p, vp, vp, vp, vp, vp, vp, u32, vp, I64p, vp,
                                               ctypes.c_size_t, vp]),
         "gdn_prefill_chunks_noalloc": (ctypes.c_int, [D, Sp, vp, vp, vp, vp, vp, vp, i64, u32, vp, I64p, vp]),
+        "gdn_prefill_branches": (ctypes.c_int, [D, Sp, Sp, i32, I64p, vp, vp, vp, vp, vp, vp, u32, vp, I64p, vp,
+                                                ctypes.c_size_t, vp]),
         "gdn_state_capture": (ctypes.c_int, [D, Sp, Sp, vp]),
         "gdn_state_restore": (ctypes.c_int, [D, Sp, Sp, vp]),
         "gdn_conv_state": (ctypes.c_int, [D, Sp, vp, vp]),
@@ -242,6 +244,22 @@ def gdn_prefill_varlen(desc, sessions: Sequence[Session], cu_seqlens: Sequence[i
         ctypes.byref(desc), arr, n, cu, _ptr(xq), _ptr(xk), _ptr(xv), _ptr(g), _ptr(beta), _ptr(conv_w),
         flags, _ptr(out), nc, _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream))
     for i, s in enumerate(sessions):   # the library updated the copies in `arr`
+        s.c.committed = arr[i].committed
+    _check(st)
+    return [int(x) for x in nc]
+
+
+def gdn_prefill_branches(desc, prefix: Session, branches: Sequence[Session], cu_seqlens: Sequence[int], xq, xk, xv,
+                         g, beta, conv_w, out, ws: torch.Tensor, flags: int = 0, stream=None) -> List[int]:
+    """Every branch continues `prefix` (read in place, unchanged) with its own packed rows."""
+    n = len(branches)
+    arr = (gdn_session * n)(*[s.c for s in branches])
+    cu = (ctypes.c_int64 * (n + 1))(*[int(x) for x in cu_seqlens])
+    nc = (ctypes.c_int64 * n)()
+    st = load_library().gdn_prefill_branches(
+        ctypes.byref(desc), ctypes.byref(prefix.c), arr, n, cu, _ptr(xq), _ptr(xk), _ptr(xv), _ptr(g), _ptr(beta),
+        _ptr(conv_w), flags, _ptr(out), nc, _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream))
+    for i, s in enumerate(branches):
         s.c.committed = arr[i].committed
     _check(st)
     return [int(x) for x in nc]

@@ -147,6 +147,24 @@ gdn_status gdn_prefill_varlen(const gdn_layer_desc *desc, gdn_session *sessions,
                               const void *conv_w, uint32_t flags, void *out, int64_t *n_consumed,
                               void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/* Prefill of n_branches branches that all continue one prefix: branch i's
+ * tokens are rows [cu_seqlens[i], cu_seqlens[i+1]) of the packed inputs (as in
+ * gdn_prefill_varlen). Every branch starts from the prefix session's state,
+ * which the kernels read in place (no copy per branch) and never change; the
+ * branch's own buffers receive its result, and its committed becomes the
+ * prefix's plus what it consumed. Branch i's result is bit-identical to
+ * gdn_state_restore(branch i, prefix) followed by gdn_prefill_chunks on its
+ * tokens (the shared-prefix continuation of "The shadow reader" and of
+ * "Long context and sessions", section "Checkpoints"). A branch with nothing
+ * to process becomes a copy of the prefix. The grid rule applies to the
+ * prefix's committed length. Branches and the prefix must be distinct
+ * sessions; a branch may be a missing slot (committed < 0) of this layer. */
+gdn_status gdn_prefill_branches(const gdn_layer_desc *desc, const gdn_session *prefix, gdn_session *branches,
+                                int32_t n_branches, const int64_t *cu_seqlens, const void *xq, const void *xk,
+                                const void *xv, const float *g, const float *beta, const void *conv_w,
+                                uint32_t flags, void *out, int64_t *n_consumed, void *workspace,
+                                size_t workspace_bytes, gdn_stream_t stream);
+
 /* Bytes of the library's built-in scratch used by gdn_prefill_chunks_noalloc
  * (held on every GPU that loads the library, until the process exits). */
 #define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)

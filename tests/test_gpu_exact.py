@@ -236,3 +236,45 @@ def test_shared_prefix_branches_equal_full_pass(cuda_device):
     _, res2 = _shared_prefix_run(w, cw, cuda_device, reverse=True)
     for k, v in res.items():
         assert _same(v[2], res2[k][2]) and _same(v[3], res2[k][3])
+
+
+def test_branches_in_one_call_equal_restore_and_prefill(cuda_device):
+    """All branches of a group in one gdn_prefill_branches call, reading the group's state in place, equal
+    the restore-then-prefill results bit for bit; an empty branch becomes a copy of the prefix, which is
+    left unchanged."""
+    w = wl.shared_prefix()
+    cw = w.conv_weights()
+    run, res = _shared_prefix_run(w, cw, cuda_device)
+    desc, shape = run.desc, w.shape
+    R, cut = w.request_prefix, wl.grid_floor(w.request_prefix, 64)
+    req = w.session_tokens(0, R)
+    xs = lambda toks: wl.tokens_to_torch(toks, shape.dtype, cuda_device)
+    for g, gp in enumerate(w.group_prefixes):
+        prompt = wl.Tokens.concat([req, w.extra_tokens(g, gp)])
+        gcut = wl.grid_floor(R + gp, 64)
+        gstate = run.session()
+        x = xs(prompt.slice(0, gcut))
+        assert gdn.gdn_prefill_chunks(desc, gstate, *x, run.cw_t, run.new_out(gcut), run.ws) == gcut
+        S_before, conv_before = gstate.S.clone(), gstate.conv.clone()
+        tails = [res[(g, b)][0].slice(gcut, len(res[(g, b)][0])) for b in range(len(w.branches[g]))]
+        tails.append(prompt.slice(gcut, gcut))   # an empty branch
+        cu = [0]
+        for t in tails:
+            cu.append(cu[-1] + len(t))
+        packed = xs(wl.Tokens.concat(tails))
+        out = torch.full((cu[-1], shape.n_v_heads, shape.d_v), float("nan"), device=cuda_device)
+        branches = [run.session() for _ in tails]
+        ws = gdn.workspace(desc, cu[-1] + 64 * len(tails), len(tails), cuda_device)
+        n = gdn.gdn_prefill_branches(desc, gstate, branches, cu, *packed, run.cw_t, out, ws,
+                                     flags=gdn.GDN_ALLOW_PARTIAL)
+        assert n == [len(t) for t in tails]
+        torch.cuda.synchronize()
+        for b in range(len(tails) - 1):
+            bt, bcut, ob, S, conv = res[(g, b)]
+            assert bcut == gcut
+            assert _same(out[cu[b]:cu[b + 1]], ob), (g, b)
+            assert _same(branches[b].S, S) and _same(branches[b].conv, conv), (g, b)
+            assert branches[b].committed == len(bt)
+        empty = branches[-1]
+        assert empty.committed == gcut and _same(empty.S, S_before) and _same(empty.conv, conv_before)
+        assert _same(gstate.S, S_before) and _same(gstate.conv, conv_before) and gstate.committed == gcut
