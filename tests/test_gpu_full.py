@@ -191,3 +191,41 @@ def _embed_conv(cs_sub, v_heads, sh):
     cs = np.zeros((3, sh.channels))
     cs[:, chan] = cs_sub
     return cs
+
+
+def test_grid_2048_replay_and_grid_independence(cuda_device):
+    """Grid 2,048 on the replay tokens: turn-by-turn replay equals a fresh call bit for bit, and, since the
+    grid sets only the commit granularity and the 64-token block the arithmetic, both equal the grid-512
+    results at the common committed length."""
+    w = wl.qwen08b_replay()
+    tok, cw = w.session_tokens(0), w.conv_weights()
+    sh2048 = wl.Shape(w.shape.n_qk_heads, w.shape.n_v_heads, w.shape.d_k, w.shape.d_v, 2048, w.shape.dtype)
+    run = Runner(sh2048, tok, cw, cuda_device)
+    o_rep, o_fresh = run.new_out(), run.new_out()
+    rep, fresh = run.session(), run.session()
+    end = 0
+    for n in w.turns[0]:
+        end += n
+        run.prefill(rep, rep.committed, end, o_rep)
+    n = run.prefill(fresh, 0, len(tok), o_fresh)
+    assert rep.committed == fresh.committed == n == 20 * 2048
+    assert _same(o_rep[:n], o_fresh[:n]) and _same(rep.S, fresh.S) and _same(rep.conv, fresh.conv)
+    run512 = Runner(w.shape, tok, cw, cuda_device)
+    s512, o512 = run512.session(), run512.new_out()
+    assert run512.prefill(s512, 0, n, o512) == n
+    assert _same(o512[:n], o_fresh[:n]) and _same(s512.S, fresh.S) and _same(s512.conv, fresh.conv)
+
+
+def test_silu_and_q_scale_on_the_replay(cuda_device):
+    """The replay tokens with the SiLU conv and q scaled by d^-1/2: oracle parity on sampled heads."""
+    w = wl.qwen08b_replay()
+    tok, cw = w.session_tokens(0), w.conv_weights()
+    qs = float(w.shape.d_k) ** -0.5
+    run = Runner(w.shape, tok, cw, cuda_device, act=gdn.GDN_CONV_SILU, q_scale=qs)
+    sess, out = run.session(), run.new_out()
+    n = run.prefill(sess, 0, len(tok), out)
+    heads = [5, 14]
+    o_ref, ST_ref, _ = oracle_run(w.shape, tok.slice(0, n), cw, v_heads=heads, act=1, q_scale=qs)
+    tol_o, tol_s = TOL[w.shape.dtype]
+    assert out_rel(out[:n][:, heads].double().cpu().numpy(), o_ref) <= tol_o
+    assert rel_l2_max(sess.S[heads].double().cpu().numpy(), ST_ref) <= tol_s
