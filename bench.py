@@ -4,9 +4,10 @@
 Default workload: the Qwen3.5-0.8B-shaped layer (16 heads, d_k = d_v = 128,
 grid C = 512, bf16 inputs, fp32 state and outputs), one session of 41,802
 synthetic tokens fed as 30 turns of 200..4,000 tokens with the sub-grid tail
-held pending, a checkpoint captured at every turn end (6 rotating slots), and
-at the end one fork that prefills the 330-token pending tail plus a 290-token
-question and restores the state ("The shadow reader", sections "One session's
+held pending, a checkpoint of every turn's end state (6 rotating slots, written
+by the turn's own prefill call), and at the end one fork that prefills the
+330-token pending tail plus a 290-token question and restores the state from
+the last turn's checkpoint ("The shadow reader", sections "One session's
 state", "Exact on a grid" and "Who asks"). One step = that whole sequence.
 
 Prints one JSON line. `value` = tokens processed per second with inputs
@@ -214,7 +215,6 @@ class ReplayStep:
         self.ws = gdn.workspace(self.desc, max_call, 1, device)
         self.sess = gdn.Session(self.desc, device)
         self.slots = [gdn.Session(self.desc, device) for _ in range(w.n_slots)]
-        self.fork_slot = gdn.Session(self.desc, device)
         self.tokens_per_step = committed + (self.rows - committed)
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host) + \
             self.host_cw.numel() * self.host_cw.element_size()
@@ -224,15 +224,16 @@ class ReplayStep:
         g = self.gdn
         d, s, x, cw, out, ws = self.desc, self.sess, self.x, self.cw, self.out, self.ws
         g.gdn_session_init(d, s)
-        for k, (a, b, take) in enumerate(self.calls):
-            n = g.gdn_prefill_chunks(d, s, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b], cw, out[a:b], ws)
+        for k, (a, b, take) in enumerate(self.calls):   # each turn keeps a checkpoint of its end state
+            slot = self.slots[k % len(self.slots)]
+            n = g.gdn_prefill_chunks_checkpoint(d, s, slot, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b],
+                                                cw, out[a:b], ws)
             assert n == take
-            g.gdn_state_capture(d, s, self.slots[k % len(self.slots)])
-        g.gdn_state_capture(d, s, self.fork_slot)
+        # the fork: tail + question above the committed rows, then back to the last turn's checkpoint
         a, b = self.fork
         g.gdn_prefill_chunks(d, s, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b], cw, out[a:b], ws,
                              flags=g.GDN_ALLOW_PARTIAL)
-        g.gdn_state_restore(d, s, self.fork_slot)
+        g.gdn_state_restore(d, s, slot)
 
     def _e2e_setup(self):
         """Copy plan of the end-to-end step: per turn, the new input rows (host -> device) and the output rows
@@ -284,16 +285,16 @@ class ReplayStep:
         g.gdn_session_init(d, s)
         for k, (a, b, take) in enumerate(self.calls):
             rt.wait(comp, ev[k])
-            n = g.gdn_prefill_chunks(d, s, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b], cw, out[a:b], ws)
+            slot = self.slots[k % len(self.slots)]
+            n = g.gdn_prefill_chunks_checkpoint(d, s, slot, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b],
+                                                cw, out[a:b], ws)
             assert n == take
-            g.gdn_state_capture(d, s, self.slots[k % len(self.slots)])
             download(k, self.plan[k][1])
-        g.gdn_state_capture(d, s, self.fork_slot)
         a, b = self.fork
         rt.wait(comp, ev[n_calls])
         g.gdn_prefill_chunks(d, s, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b], cw, out[a:b], ws,
                              flags=g.GDN_ALLOW_PARTIAL)
-        g.gdn_state_restore(d, s, self.fork_slot)
+        g.gdn_state_restore(d, s, slot)
         download(n_calls, self.plan_fork[1])
         rt.record(ev[-2], d2h)
         rt.wait(comp, ev[-2])

@@ -291,10 +291,15 @@ namespace {
 gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t n_sessions, const int64_t *cu,
                         const void *xq, const void *xk, const void *xv, const float *g, const float *beta,
                         const void *conv_w, uint32_t flags, void *out, int64_t *n_consumed, void *workspace,
-                        size_t workspace_bytes, gdn_stream_t stream, const gdn_session *prefix) {
+                        size_t workspace_bytes, gdn_stream_t stream, const gdn_session *prefix,
+                        gdn_session *ckpt) {
     gdn_status st = check_desc(d);
     if (st != GDN_OK) return st;
     if (prefix && (st = check_state(d, prefix, "prefix", true)) != GDN_OK) return st;
+    if (ckpt && n_sessions >= 1)
+        for (int i = 0; i < n_sessions; ++i)
+            if (!ckpt[i].S || !ckpt[i].conv || !aligned16(ckpt[i].S) || !aligned16(ckpt[i].conv))
+                return fail(GDN_ERR_INVALID_ARG, "checkpoint slot %d: buffers must be non-NULL and 16-byte aligned", i);
     if (flags & ~GDN_ALLOW_PARTIAL) return fail(GDN_ERR_INVALID_ARG, "unknown flags 0x%x", flags);
     if (n_sessions < 1 || n_sessions > GDN_MAX_SESSIONS)
         return fail(GDN_ERR_INVALID_ARG, "n_sessions must be in [1, %d] (got %d)", GDN_MAX_SESSIONS, n_sessions);
@@ -322,10 +327,12 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
         std::vector<const void *> ptrs(n_sessions);
         for (int i = 0; i < n_sessions; ++i) ptrs[i] = sessions[i].S;
         if (prefix) ptrs.push_back(prefix->S);
+        if (ckpt)
+            for (int i = 0; i < n_sessions; ++i) ptrs.push_back(ckpt[i].S);
         std::sort(ptrs.begin(), ptrs.end());
         if (std::adjacent_find(ptrs.begin(), ptrs.end()) != ptrs.end())
-            return fail(GDN_ERR_INVALID_ARG, prefix ? "the branches and the prefix must be distinct sessions"
-                                                    : "the sessions of one call must be distinct");
+            return fail(GDN_ERR_INVALID_ARG, prefix ? "the branches, the prefix and the checkpoints must be distinct"
+                                                    : "the sessions and checkpoints of one call must be distinct");
     }
     // blocks per launch batch, and the workspace that needs
     int64_t max_batch_blocks = 0;
@@ -357,7 +364,8 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
     cudaStream_t cst = (cudaStream_t)stream;
     if (total > 0) {
         const WsLayout L = ws_layout(d, max_batch_blocks);
-        static_assert(sizeof(LaunchCommon) <= 4096, "launch parameters must fit the 4 KB limit");
+        // kernel parameters may take up to 32,764 bytes (compute capability 7.0+, CUDA 12.1+)
+        static_assert(sizeof(LaunchCommon) <= 32764, "launch parameters must fit the kernel-parameter limit");
         LaunchCommon p;
         fill_common(p, d, xq, xk, xv, g, beta, conv_w, out);
         p.ws_qk = reinterpret_cast<float *>(ws_base(workspace) + L.qk_off);
@@ -378,6 +386,8 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
                 r.S = sessions[i].S; r.conv = sessions[i].conv;
                 r.S0 = prefix ? prefix->S : r.S;
                 r.conv0 = prefix ? prefix->conv : r.conv;
+                r.S_cap = ckpt ? static_cast<float *>(ckpt[i].S) : nullptr;
+                r.conv_cap = ckpt ? ckpt[i].conv : nullptr;
                 blk += (int)((nproc[i] + kBlock - 1) / kBlock);
             }
             i0 = i;
@@ -401,20 +411,29 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
             if (e != cudaSuccess) return cuda_fail(e, "state/output kernel");
         }
     }
-    if (prefix) {   // a branch with nothing to process becomes a copy of the prefix
+    {   // sessions with nothing to process: a branch becomes a copy of the prefix, a checkpoint a copy of the
+        // session's (unchanged) state
         cudaStream_t cst = (cudaStream_t)stream;
         for (int i = 0; i < n_sessions; ++i) {
             if (nproc[i] > 0) continue;
-            cudaError_t e = launch_k(K_COPY, cst, [&] {
-                return gdn_launch_copy(sessions[i].S, prefix->S, gdn_state_bytes(d), sessions[i].conv, prefix->conv,
-                                       gdn_conv_state_bytes(d), cst);
-            });
-            if (e != cudaSuccess) return cuda_fail(e, "prefix copy");
+            const gdn_session &from = prefix ? *prefix : sessions[i];
+            for (gdn_session *to : {prefix ? &sessions[i] : nullptr, ckpt ? &ckpt[i] : nullptr}) {
+                if (!to) continue;
+                cudaError_t e = launch_k(K_COPY, cst, [&] {
+                    return gdn_launch_copy(to->S, from.S, gdn_state_bytes(d), to->conv, from.conv,
+                                           gdn_conv_state_bytes(d), cst);
+                });
+                if (e != cudaSuccess) return cuda_fail(e, "state copy");
+            }
         }
     }
     for (int i = 0; i < n_sessions; ++i) {
         sessions[i].committed = (prefix ? prefix->committed : sessions[i].committed) + nproc[i];
         n_consumed[i] = nproc[i];
+        if (ckpt) {
+            ckpt[i].committed = sessions[i].committed;
+            ckpt[i].tag = tag_of(d);
+        }
     }
     return GDN_OK;
 }
@@ -427,7 +446,18 @@ GDN_API gdn_status gdn_prefill_varlen(const gdn_layer_desc *d, gdn_session *sess
                                       void *out, int64_t *n_consumed, void *workspace, size_t workspace_bytes,
                                       gdn_stream_t stream) {
     return prefill_impl(d, sessions, n_sessions, cu, xq, xk, xv, g, beta, conv_w, flags, out, n_consumed, workspace,
-                        workspace_bytes, stream, nullptr);
+                        workspace_bytes, stream, nullptr, nullptr);
+}
+
+GDN_API gdn_status gdn_prefill_varlen_checkpoint(const gdn_layer_desc *d, gdn_session *sessions,
+                                                 gdn_session *checkpoints, int32_t n_sessions, const int64_t *cu,
+                                                 const void *xq, const void *xk, const void *xv, const float *g,
+                                                 const float *beta, const void *conv_w, uint32_t flags, void *out,
+                                                 int64_t *n_consumed, void *workspace, size_t workspace_bytes,
+                                                 gdn_stream_t stream) {
+    if (!checkpoints) return fail(GDN_ERR_INVALID_ARG, "checkpoints is NULL");
+    return prefill_impl(d, sessions, n_sessions, cu, xq, xk, xv, g, beta, conv_w, flags, out, n_consumed, workspace,
+                        workspace_bytes, stream, nullptr, checkpoints);
 }
 
 GDN_API gdn_status gdn_prefill_branches(const gdn_layer_desc *d, const gdn_session *prefix, gdn_session *branches,
@@ -437,7 +467,7 @@ GDN_API gdn_status gdn_prefill_branches(const gdn_layer_desc *d, const gdn_sessi
                                         size_t workspace_bytes, gdn_stream_t stream) {
     if (!prefix) return fail(GDN_ERR_INVALID_ARG, "prefix is NULL");
     return prefill_impl(d, branches, n_branches, cu, xq, xk, xv, g, beta, conv_w, flags, out, n_consumed, workspace,
-                        workspace_bytes, stream, prefix);
+                        workspace_bytes, stream, prefix, nullptr);
 }
 
 GDN_API gdn_status gdn_prefill_chunks(const gdn_layer_desc *d, gdn_session *session, const void *xq,
@@ -449,6 +479,17 @@ GDN_API gdn_status gdn_prefill_chunks(const gdn_layer_desc *d, gdn_session *sess
     const int64_t cu[2] = {0, n_tokens};
     return gdn_prefill_varlen(d, session, 1, cu, xq, xk, xv, g, beta, conv_w, flags, out, n_consumed, workspace,
                               workspace_bytes, stream);
+}
+
+GDN_API gdn_status gdn_prefill_chunks_checkpoint(const gdn_layer_desc *d, gdn_session *session, gdn_session *slot,
+                                                 const void *xq, const void *xk, const void *xv, const float *g,
+                                                 const float *beta, const void *conv_w, int64_t n_tokens,
+                                                 uint32_t flags, void *out, int64_t *n_consumed, void *workspace,
+                                                 size_t workspace_bytes, gdn_stream_t stream) {
+    if (n_tokens < 0) return fail(GDN_ERR_INVALID_ARG, "n_tokens must be >= 0 (got %lld)", (long long)n_tokens);
+    const int64_t cu[2] = {0, n_tokens};
+    return gdn_prefill_varlen_checkpoint(d, session, slot, 1, cu, xq, xk, xv, g, beta, conv_w, flags, out, n_consumed,
+                                         workspace, workspace_bytes, stream);
 }
 
 GDN_API gdn_status gdn_state_capture(const gdn_layer_desc *d, const gdn_session *src, gdn_session *slot,

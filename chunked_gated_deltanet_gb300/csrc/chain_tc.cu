@@ -69,6 +69,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
             }
 #pragma unroll
             for (int r = 0; r < 3; ++r) cs[r * ch + chan] = nw[r];
+            if (s.conv_cap) {
+                __nv_bfloat16 *cc = static_cast<__nv_bfloat16 *>(s.conv_cap);
+#pragma unroll
+                for (int r = 0; r < 3; ++r) cc[r * ch + chan] = nw[r];
+            }
         }
     }
 
@@ -236,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
         __syncthreads();
         return;
     }
+    float *Scap = s.S_cap ? s.S_cap + (int64_t)h * D * D : nullptr;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int c = 8 * nt + 2 * t4;
@@ -244,6 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
             Sg[(int64_t)m0 * D + c0 + c + 1] = st[nt][1];
             Sg[(int64_t)(m0 + 8) * D + c0 + c] = st[nt][2];
             Sg[(int64_t)(m0 + 8) * D + c0 + c + 1] = st[nt][3];
+            if (Scap) {   // the checkpoint of this call's final state
+                Scap[(int64_t)m0 * D + c0 + c] = st[nt][0];
+                Scap[(int64_t)m0 * D + c0 + c + 1] = st[nt][1];
+                Scap[(int64_t)(m0 + 8) * D + c0 + c] = st[nt][2];
+                Scap[(int64_t)(m0 + 8) * D + c0 + c + 1] = st[nt][3];
+            }
         }
     }
 }

@@ -21,6 +21,8 @@ struct SessRef {
     void *conv;      // in_dtype [3][ch] conv state: the result goes here
     const float *S0;      // the state the call starts from (S itself, or a shared prefix's state)
     const void *conv0;    // the conv state it starts from (conv itself, or the prefix's)
+    float *S_cap;         // optional checkpoint: the final state is also written here (null: none)
+    void *conv_cap;       // and the final conv state here
 };
 
 struct LaunchCommon {

@@ -29,6 +29,11 @@ __global__ void __launch_bounds__(256) conv_commit_kernel(const LaunchCommon p, 
     }
 #pragma unroll
     for (int r = 0; r < 3; ++r) cs[r * ch + chan] = nw[r];
+    if (s.conv_cap) {
+        InT *cc = static_cast<InT *>(s.conv_cap);
+#pragma unroll
+        for (int r = 0; r < 3; ++r) cc[r * ch + chan] = nw[r];
+    }
 }
 
 // Two independent 16-byte-vector copies in one launch; a null source zero-fills.

@@ -110,6 +110,10 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const LaunchCommon p
     }
     __syncthreads();
     for (int e = t; e < D * DS; e += kThreads) Sg[(e / DS) * D + c0 + e % DS] = St[e];
+    if (s.S_cap) {   // the checkpoint of this call's final state
+        float *Sc = s.S_cap + (int64_t)h * D * D;
+        for (int e = t; e < D * DS; e += kThreads) Sc[(e / DS) * D + c0 + e % DS] = St[e];
+    }
 }
 
 template <int D>

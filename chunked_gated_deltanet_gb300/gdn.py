@@ -37,7 +37,8 @@ EXPORTED = ["gdn_desc_tag", "gdn_desc_check", "gdn_state_bytes", "gdn_conv_state
             "gdn_state_restore", "gdn_conv_state", "gdn_decode_step", "gdn_timing_begin", "gdn_timing_end",
             "gdn_prefill_chunks_noalloc", "gdn_device_status", "gdn_debug_inject_wait_timeout",
             "gdn_last_error", "gdn_status_string", "gdn_state_blob_bytes", "gdn_state_serialize",
-            "gdn_state_deserialize", "gdn_state_save", "gdn_state_load", "gdn_prefill_branches"]
+            "gdn_state_deserialize", "gdn_state_save", "gdn_state_load", "gdn_prefill_branches",
+            "gdn_prefill_chunks_checkpoint", "gdn_prefill_varlen_checkpoint"]
 
 
 class gdn_layer_desc(ctypes.Structure):
@@ -93,6 +94,10 @@ def load_library(path: Optional[str] = None):
         "gdn_prefill_chunks_noalloc": (ctypes.c_int, [D, Sp, vp, vp, vp, vp, vp, vp, i64, u32, vp, I64p, vp]),
         "gdn_prefill_branches": (ctypes.c_int, [D, Sp, Sp, i32, I64p, vp, vp, vp, vp, vp, vp, u32, vp, I64p, vp,
                                                 ctypes.c_size_t, vp]),
+        "gdn_prefill_chunks_checkpoint": (ctypes.c_int, [D, Sp, Sp, vp, vp, vp, vp, vp, vp, i64, u32, vp, I64p, vp,
+                                                         ctypes.c_size_t, vp]),
+        "gdn_prefill_varlen_checkpoint": (ctypes.c_int, [D, Sp, Sp, i32, I64p, vp, vp, vp, vp, vp, vp, u32, vp, I64p,
+                                                         vp, ctypes.c_size_t, vp]),
         "gdn_state_capture": (ctypes.c_int, [D, Sp, Sp, vp]),
         "gdn_state_restore": (ctypes.c_int, [D, Sp, Sp, vp]),
         "gdn_conv_state": (ctypes.c_int, [D, Sp, vp, vp]),
@@ -245,6 +250,37 @@ def gdn_prefill_varlen(desc, sessions: Sequence[Session], cu_seqlens: Sequence[i
         flags, _ptr(out), nc, _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream))
     for i, s in enumerate(sessions):   # the library updated the copies in `arr`
         s.c.committed = arr[i].committed
+    _check(st)
+    return [int(x) for x in nc]
+
+
+def gdn_prefill_chunks_checkpoint(desc, sess: Session, slot: Session, xq, xk, xv, g, beta, conv_w, out,
+                                  ws: torch.Tensor, flags: int = 0, n_tokens: Optional[int] = None, stream=None) -> int:
+    """gdn_prefill_chunks, with the result also written into `slot` in the same pass."""
+    n_tokens = xq.shape[0] if n_tokens is None else n_tokens
+    nc = ctypes.c_int64(0)
+    st = load_library().gdn_prefill_chunks_checkpoint(
+        ctypes.byref(desc), ctypes.byref(sess.c), ctypes.byref(slot.c), _ptr(xq), _ptr(xk), _ptr(xv), _ptr(g),
+        _ptr(beta), _ptr(conv_w), n_tokens, flags, _ptr(out), ctypes.byref(nc), _ptr(ws),
+        ws.numel() if ws is not None else 0, _stream(stream))
+    _check(st)
+    return int(nc.value)
+
+
+def gdn_prefill_varlen_checkpoint(desc, sessions: Sequence[Session], slots: Sequence[Session],
+                                  cu_seqlens: Sequence[int], xq, xk, xv, g, beta, conv_w, out, ws: torch.Tensor,
+                                  flags: int = 0, stream=None) -> List[int]:
+    n = len(sessions)
+    arr = (gdn_session * n)(*[s.c for s in sessions])
+    sarr = (gdn_session * n)(*[s.c for s in slots])
+    cu = (ctypes.c_int64 * (n + 1))(*[int(x) for x in cu_seqlens])
+    nc = (ctypes.c_int64 * n)()
+    st = load_library().gdn_prefill_varlen_checkpoint(
+        ctypes.byref(desc), arr, sarr, n, cu, _ptr(xq), _ptr(xk), _ptr(xv), _ptr(g), _ptr(beta), _ptr(conv_w),
+        flags, _ptr(out), nc, _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream))
+    for i in range(n):
+        sessions[i].c.committed = arr[i].committed
+        slots[i].c.committed, slots[i].c.tag = sarr[i].committed, sarr[i].tag
     _check(st)
     return [int(x) for x in nc]
 

@@ -147,6 +147,26 @@ gdn_status gdn_prefill_varlen(const gdn_layer_desc *desc, gdn_session *sessions,
                               const void *conv_w, uint32_t flags, void *out, int64_t *n_consumed,
                               void *workspace, size_t workspace_bytes, gdn_stream_t stream);
 
+/* gdn_prefill_chunks (gdn_prefill_varlen) that also writes each session's
+ * result into a checkpoint slot, as gdn_state_capture(session -> slot) after
+ * the call would, but in the same pass: the state kernel stores the final
+ * state and conv state twice, and no copy launch follows. A turn of a
+ * conversation that keeps a checkpoint at every turn end is one call ("The
+ * shadow reader": a checkpoint of the recurrent state at each turn's prompt
+ * end). Slots need buffers of this layer, distinct from every session and
+ * from each other; their committed and tag are set as a capture sets them.
+ * A refused call changes no slot. */
+gdn_status gdn_prefill_chunks_checkpoint(const gdn_layer_desc *desc, gdn_session *session, gdn_session *slot,
+                                         const void *xq, const void *xk, const void *xv, const float *g,
+                                         const float *beta, const void *conv_w, int64_t n_tokens, uint32_t flags,
+                                         void *out, int64_t *n_consumed, void *workspace, size_t workspace_bytes,
+                                         gdn_stream_t stream);
+gdn_status gdn_prefill_varlen_checkpoint(const gdn_layer_desc *desc, gdn_session *sessions, gdn_session *slots,
+                                         int32_t n_sessions, const int64_t *cu_seqlens, const void *xq,
+                                         const void *xk, const void *xv, const float *g, const float *beta,
+                                         const void *conv_w, uint32_t flags, void *out, int64_t *n_consumed,
+                                         void *workspace, size_t workspace_bytes, gdn_stream_t stream);
+
 /* Prefill of n_branches branches that all continue one prefix: branch i's
  * tokens are rows [cu_seqlens[i], cu_seqlens[i+1]) of the packed inputs (as in
  * gdn_prefill_varlen). Every branch starts from the prefix session's state,

@@ -278,3 +278,42 @@ def test_branches_in_one_call_equal_restore_and_prefill(cuda_device):
         empty = branches[-1]
         assert empty.committed == gcut and _same(empty.S, S_before) and _same(empty.conv, conv_before)
         assert _same(gstate.S, S_before) and _same(gstate.conv, conv_before) and gstate.committed == gcut
+
+
+@pytest.mark.parametrize("dtype,d", [(wl.BF16, 128), (wl.BF16, 64), (wl.FP32, 64)])
+def test_checkpointing_prefill_equals_prefill_then_capture(cuda_device, dtype, d):
+    """gdn_prefill_chunks_checkpoint writes into its slot exactly what a capture after the call would, and
+    leaves the session as gdn_prefill_chunks does; a call with nothing to commit checkpoints the unchanged
+    state; the varlen form does the same per session."""
+    shape = wl.Shape(2, 4, d, d, 128, dtype)
+    w = wl.Workload("ckpt", shape, seed=51, session_lengths=[700])
+    run = Runner(shape, w.session_tokens(0), w.conv_weights(), cuda_device)
+    a, b = run.session(), run.session()
+    sa, sb = run.session(), run.session()
+    oa, ob = run.new_out(), run.new_out()
+    for lo, hi in ((0, 300), (256, 600), (512, 600)):      # the last call commits nothing
+        x = [t[lo:hi] for t in run.x]
+        na = gdn.gdn_prefill_chunks(run.desc, a, *x, run.cw_t, oa[lo:hi], run.ws)
+        gdn.gdn_state_capture(run.desc, a, sa)
+        nb = gdn.gdn_prefill_chunks_checkpoint(run.desc, b, sb, *x, run.cw_t, ob[lo:hi], run.ws)
+        assert na == nb and a.committed == b.committed == sa.committed == sb.committed
+        assert sb.tag == sa.tag == a.tag
+        assert _same(oa, ob) and _same(a.S, b.S) and _same(a.conv, b.conv)
+        assert _same(sa.S, sb.S) and _same(sa.conv, sb.conv)
+    # varlen: three sessions, one checkpoint each
+    runs = [Runner(shape, wl.Workload("ckv", shape, seed=60 + i, session_lengths=[300 + 100 * i]).session_tokens(0),
+                   run.cw, cuda_device) for i in range(3)]
+    toks = [r.tok for r in runs]
+    cu = np.cumsum([0] + [len(t) for t in toks]).tolist()
+    x = wl.tokens_to_torch(wl.Tokens.concat(toks), dtype, cuda_device)
+    ws = gdn.workspace(run.desc, cu[-1] + 64 * 3, 3, cuda_device)
+    ses, slots = [run.session() for _ in range(3)], [run.session() for _ in range(3)]
+    out = torch.zeros((cu[-1], shape.n_v_heads, d), device=cuda_device)
+    gdn.gdn_prefill_varlen_checkpoint(run.desc, ses, slots, cu, *x, run.cw_t, out, ws)
+    ref = [run.session() for _ in range(3)]
+    out2 = torch.zeros_like(out)
+    gdn.gdn_prefill_varlen(run.desc, ref, cu, *x, run.cw_t, out2, ws)
+    assert _same(out, out2)
+    for s, sl, r in zip(ses, slots, ref):
+        assert sl.committed == s.committed == r.committed
+        assert _same(s.S, r.S) and _same(sl.S, r.S) and _same(sl.conv, r.conv)
