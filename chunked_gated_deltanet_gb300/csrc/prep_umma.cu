@@ -318,6 +318,20 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
         *reinterpret_cast<uint4 *>(lo + off) = l;
     };
 
+    // beta v of the staged v-head (row-parallel conv, 4 rows per warp) into channels 128..255 of the B operand
+    auto conv_v = [&]() {
+        conv_rows(rawv, wv, 4 * warp, 4, [&](int i0, float (&y)[4][4]) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                float v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = i < n ? bet[i] * y[u][c] : 0.f;
+                split4_store(Bh, Bl, mnmajor_bf16_offset(128 + 4 * lane, i, B_LBO, B_SBO), v);
+            }
+        });
+    };
+
     {   // 1. q, k and the first v-head's tiles
         const Tile tl[3] = {
             {rawq, wq, &p.tm_q, static_cast<const __nv_bfloat16 *>(p.xq), nq, (int64_t)hk * D, (int64_t)hk * D},
@@ -325,13 +339,31 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
             {rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)(hk * p.G) * D, 2 * nq + (int64_t)(hk * p.G) * D}};
         stage(tl, 3, p.debug_skip_first_copy == 2);
     }
-    // g and beta of the first v-head (warps 2 and 3 own the gamma scan; warp 0 issues the MMAs)
+    // gamma (inclusive scan of g over the block), beta and e^gamma of v-head h, by warps 2 and 3 alone while
+    // the input copies are in flight: warp 3 adds the total of rows 0..31 itself, so no barrier is needed
     const int jg = t - 64;
-    float gv = 0.f, bv = 0.f;
-    if (jg >= 0 && jg < n) {
-        gv = p.g[(row0 + jg) * Hv + hk * p.G];
-        bv = p.beta[(row0 + jg) * Hv + hk * p.G];
-    }
+    auto gates = [&](int h) {
+        if (jg < 0 || jg >= kBlock) return;
+        const float gv = jg < n ? p.g[(row0 + jg) * Hv + h] : 0.f;
+        const float bv = jg < n ? p.beta[(row0 + jg) * Hv + h] : 0.f;
+        float lo = 0.f;
+        if (jg >= 32 && lane < n) lo = p.g[(row0 + lane) * Hv + h];
+        float sv = gv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, sv, o);
+            if (lane >= o) sv += y;
+        }
+        if (jg >= 32) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lo += __shfl_xor_sync(0xffffffffu, lo, o);
+            sv += lo;
+        }
+        gam[jg] = sv;
+        bet[jg] = bv;
+        egv[jg] = expf(sv);
+    };
+    gates(hk * p.G);
     bool ok = wait_in();
 
     if (ok) {
@@ -360,6 +392,7 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
                 split4_store(AQh, AQl, kmajor_bf16_offset(64 * which + i, 4 * lane, AQ_LBO, AQ_SBO), v);
             }
         });
+        conv_v();   // the first v-head's beta v in the same phase
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -377,45 +410,35 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
         if (gi > 0) {   // the previous head is done with the raw-tile region and every MMA operand
             const Tile tl[1] = {{rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)h * D, 2 * nq + (int64_t)h * D}};
             stage(tl, 1, false);
-            gv = bv = 0.f;
-            if (jg >= 0 && jg < n) {
-                gv = p.g[(row0 + jg) * Hv + h];
-                bv = p.beta[(row0 + jg) * Hv + h];
-            }
-        }
-        if (jg >= 0 && jg < kBlock) {   // gamma: inclusive scan of g (warps 2 and 3)
-            float sv = gv;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, sv, o);
-                if (lane >= o) sv += y;
-            }
-            gam[jg] = sv;
-            bet[jg] = bv;
-        }
-        if (gi > 0) {
+            gates(h);
             if (!(ok = wait_in())) break;
-        } else {
-            __syncthreads();
         }
-        if (jg >= 32 && jg < kBlock) gam[jg] += gam[31];
-        __syncthreads();
-        if (jg >= 0 && jg < kBlock) egv[jg] = expf(gam[jg]);
-        __syncthreads();
         float *rec = p.ws_wu + ((int64_t)blk * Hv + h) * rec_floats(D);
-
-        // 5. B operand, MN-major: channels 128..255 = beta v (row-parallel conv, 4 rows per warp),
-        //    channels 0..127 = beta e^gamma k_hat (from the hi/lo rows)
-        conv_rows(rawv, wv, 4 * warp, 4, [&](int i0, float (&y)[4][4]) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u;
+        // K_tilde^T as tf32 A fragments (D x 64), half `part` of its float4 groups, by warps 1-15 (warp 0
+        // issues the MMAs); e^{gamma_63} with the first half
+        auto kt_record = [&](int part) {
+            if (warp == 0) return;
+            constexpr int NG = (D / 16) * 8 * 32, HALF = NG / 2;
+            const float gl = gam[kBlock - 1];
+            for (int e = HALF * part + t - 32; e < HALF * (part + 1); e += kUmmaPrepThreads - 32) {
+                const int ln = e & 31, tile = e >> 5, mt = tile >> 3, ks = tile & 7, gg = ln >> 2, tt = ln & 3;
                 float v[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) v[c] = i < n ? bet[i] * y[u][c] : 0.f;
-                split4_store(Bh, Bl, mnmajor_bf16_offset(128 + 4 * lane, i, B_LBO, B_SBO), v);
+                for (int f = 0; f < 4; ++f) {
+                    const int m = 16 * mt + gg + 8 * (f & 1), k = 8 * ks + tt + 4 * (f >> 1);
+                    const uint32_t o = kmajor_bf16_offset(kBlock + k, m, AQ_LBO, AQ_SBO);
+                    const float kh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQh + o)) +
+                                     __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQl + o));
+                    v[f] = tf32_round(__expf(gl - gam[k]) * kh);
+                }
+                *reinterpret_cast<float4 *>(rec + 128 * D + e * 4) = make_float4(v[0], v[1], v[2], v[3]);
             }
-        });
+            if (part == 0 && t == 32) rec[320 * D] = expf(gl);
+        };
+
+        // 5. B operand, MN-major: channels 128..255 = beta v (the first v-head's came with the q/k conv),
+        //    channels 0..127 = beta e^gamma k_hat (from the hi/lo rows)
+        if (gi > 0) conv_v();
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             const int j = t & 63, cg = (t >> 6) + 8 * it;
@@ -541,29 +564,13 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
         tc_fence_before();
         __syncthreads();
 
-        // 8. P T into TMEM columns 64..127; meanwhile K_tilde^T as tf32 A fragments (D x 64) and e^{gamma_63}
+        // 8. P T into TMEM columns 64..127; meanwhile the first half of the K_tilde^T record
         if (t == 0)
             mma3(tmem + 64, umma_smem_desc(Ph, K64_LBO, K64_SBO), umma_smem_desc(Pl, K64_LBO, K64_SBO), 2 * K64_LBO,
                  umma_smem_desc(TBh, K64_LBO, K64_SBO), umma_smem_desc(TBl, K64_LBO, K64_SBO), 2 * K64_LBO, kBlock,
                  umma_idesc_bf16(128, 64, 0, 1));
         mma_pending = 1;
-        if (warp > 0) {
-            const float gl = gam[kBlock - 1];
-            for (int e = t - 32; e < (D / 16) * 8 * 32; e += kUmmaPrepThreads - 32) {
-                const int ln = e & 31, tile = e >> 5, mt = tile >> 3, ks = tile & 7, gg = ln >> 2, tt = ln & 3;
-                float v[4];
-#pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    const int m = 16 * mt + gg + 8 * (f & 1), k = 8 * ks + tt + 4 * (f >> 1);
-                    const uint32_t o = kmajor_bf16_offset(kBlock + k, m, AQ_LBO, AQ_SBO);
-                    const float kh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQh + o)) +
-                                     __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQl + o));
-                    v[f] = tf32_round(__expf(gl - gam[k]) * kh);
-                }
-                *reinterpret_cast<float4 *>(rec + 128 * D + e * 4) = make_float4(v[0], v[1], v[2], v[3]);
-            }
-            if (t == 32) rec[320 * D] = expf(gl);
-        }
+        kt_record(0);   // the first half of K_tilde^T while the product runs, the second under the next one
         if (!(ok = wait_mma())) break;
 
         // 9. P T (lanes 0..63; warps 0,1,4,5,8,9,12,13, 16 columns each) -> rows 64..127 of [T; P T]
@@ -584,6 +591,7 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
                  umma_smem_desc(Bh, B_LBO, B_SBO), umma_smem_desc(Bl, B_LBO, B_SBO), 2 * B_LBO, kBlock,
                  umma_idesc_bf16(128, 256, 0, 1));
         mma_pending = 1;
+        kt_record(1);
         if (!(ok = wait_mma())) break;
 
         // 11. the record, every warp (lanes 32 (warp % 4) .., 64 columns at 64 (warp / 4)):
