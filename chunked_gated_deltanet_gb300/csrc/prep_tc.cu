@@ -1,5 +1,7 @@
-// Prologue + WY/UT transform on tensor cores (bf16 inputs), one CTA per
-// (64-token block, q/k head), for each of the head's G v-heads.
+// Prologue + WY/UT transform on the warp-level tensor-core path (mma.sync),
+// bf16 inputs, d_k = d_v = 64 (d = 128 runs the tcgen05 prologue,
+// prep_umma.cu). One CTA per (64-token block, q/k head), for each of the
+// head's G v-heads.
 //
 // Per block (rows i = 0..63; rows >= n are padding and zero everywhere):
 //   conv (kernel 4, halo from the conv state at a call's first block), L2 norm
@@ -453,5 +455,6 @@ static cudaError_t launch(const LaunchCommon &p, int64_t ch, cudaStream_t st) {
 }  // namespace gdn
 
 cudaError_t gdn_launch_prep_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st) {
-    return D == 64 ? gdn::launch<64>(p, ch, st) : gdn::launch<128>(p, ch, st);
+    if (D != 64) return cudaErrorInvalidValue;   // d = 128 has its own prologue
+    return gdn::launch<64>(p, ch, st);
 }

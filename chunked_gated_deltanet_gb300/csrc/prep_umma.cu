@@ -300,7 +300,13 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
             for (int u = 0; u < 4; ++u)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    y[u][c] = conv_tap<__nv_bfloat16>(w[c], x[u][c], x[u + 1][c], x[u + 2][c], x[u + 3][c], p.act);
+                    y[u][c] = conv_tap<__nv_bfloat16>(w[c], x[u][c], x[u + 1][c], x[u + 2][c], x[u + 3][c], 0);
+            if (p.act) {   // SiLU, as one branch after the taps so that the default path stays compact
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) y[u][c] = y[u][c] / (1.0f + expf(-y[u][c]));
+            }
             emit(i0, y);
         }
     };
@@ -602,18 +608,11 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
             const bool top = R < kBlock;
             const int i = top ? R : R - kBlock;
             const uint32_t tb = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 + 64 * cp;
-            uint32_t ra[16], rb[16];   // chunk cc in one, chunk cc + 1 in flight into the other
-            tmem_ld16_nowait(tb, ra);
-            tmem_wait_ld(ra);
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
-                uint32_t(&cur)[16] = (cc & 1) ? rb : ra;
-                uint32_t(&nxt)[16] = (cc & 1) ? ra : rb;
-                if (cc < 3) tmem_ld16_nowait(tb + 16 * (cc + 1), nxt);
                 const int c0 = 64 * cp + 16 * cc;
                 float v[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) v[c] = __uint_as_float(cur[c]);
+                tmem_ld16(tb + 16 * cc, v);
                 if (c0 < D) {
                     if (top) {
 #pragma unroll
@@ -633,7 +632,6 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
                 } else {
                     put_cfrag16(rec + (top ? 192 : 256) * D, i, c0 - D, v, lane);
                 }
-                if (cc < 3) tmem_wait_ld(nxt);
             }
         }
         tc_fence_before();
