@@ -85,6 +85,39 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tf32_tflops_probe(dev, n: int = 8192, reps: int = 10) -> float:
+    """Dense tf32 matmul rate of this GPU, measured now (the state kernel's contractions run on tf32)."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        for _ in range(3):
+            a @ b
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            a @ b
+        e1.record()
+        torch.cuda.synchronize()
+        return 2.0 * n ** 3 * reps / (e0.elapsed_time(e1) / 1e3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -216,6 +249,8 @@ class ReplayStep:
         self.sess = gdn.Session(self.desc, device)
         self.slots = [gdn.Session(self.desc, device) for _ in range(w.n_slots)]
         self.tokens_per_step = committed + (self.rows - committed)
+        # dependent 64-token block steps of one head's state pass per bench step
+        self.block_steps_per_step = sum(-(-take // 64) for _, _, take in self.calls) + -(-(self.rows - committed) // 64)
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host) + \
             self.host_cw.numel() * self.host_cw.element_size()
         self.d2h_bytes = self.out.numel() * self.out.element_size()
@@ -308,6 +343,119 @@ class ReplayStep:
                 "outputs": "fp32",
                 "l2": f"inputs larger than L2 ({self.h2d_bytes / 1e6:.0f} MB read per step vs 129 MB L2)",
                 "parallelism": "replicas"}
+
+
+class VarlenStep:
+    """8 sessions (Hk 16, Hv 32, grid 512) fed in 6 turn rounds: one varlen call per round, which also writes
+    every session's round checkpoint into that round's slot; pending tails carried between rounds."""
+
+    def __init__(self, w, device):
+        import torch
+        from chunked_gated_deltanet_gb300 import gdn
+        from chunked_gated_deltanet_gb300 import workloads as wl
+        self.gdn, self.w = gdn, w
+        sh = w.shape
+        self.desc = gdn.make_desc(sh.n_qk_heads, sh.n_v_heads, sh.d_k, sh.d_v, sh.grid_c, gdn.GDN_BF16, gdn.GDN_FP32)
+        n, C, R = len(w.session_lengths), sh.grid_c, len(w.turns[0])
+        toks = [w.session_tokens(i) for i in range(n)]
+        ends, committed = [0] * n, [0] * n
+        self.rounds, max_rows, self.block_steps_per_step = [], 0, 0
+        for r in range(R):
+            parts, cu, longest = [], [0], 0
+            for i in range(n):
+                ends[i] += w.turns[i][r]
+                parts.append(toks[i].slice(committed[i], ends[i]))
+                cu.append(cu[-1] + ends[i] - committed[i])
+                take = (ends[i] - committed[i]) // C * C
+                longest = max(longest, -(-take // 64))
+                committed[i] += take
+            x = wl.tokens_to_torch(wl.Tokens.concat(parts), sh.dtype, device)
+            out = torch.empty((cu[-1], sh.n_v_heads, sh.d_v), dtype=torch.float32, device=device)
+            self.rounds.append((cu, x, out))
+            max_rows = max(max_rows, cu[-1])
+            self.block_steps_per_step += longest
+        self.tokens_per_step = sum(committed)
+        self.cw = wl.to_torch(w.conv_weights(), sh.dtype, device)
+        self.ws = gdn.workspace(self.desc, max_rows + 64 * n, n, device)
+        self.sess = [gdn.Session(self.desc, device) for _ in range(n)]
+        self.slots = [[gdn.Session(self.desc, device) for _ in range(n)] for _ in range(R)]
+        self.n = n
+
+    def step(self):
+        g = self.gdn
+        for s in self.sess:
+            g.gdn_session_init(self.desc, s)
+        for r, (cu, x, out) in enumerate(self.rounds):
+            g.gdn_prefill_varlen_checkpoint(self.desc, self.sess, self.slots[r], cu, *x, self.cw, out, self.ws)
+
+    def config(self):
+        sh = self.w.shape
+        return {"workload": self.w.name, "sessions": self.n, "session_tokens": list(self.w.session_lengths),
+                "turn_rounds": len(self.rounds), "checkpoint_slots": len(self.slots), "tokens_per_step":
+                self.tokens_per_step, "n_qk_heads": sh.n_qk_heads, "n_v_heads": sh.n_v_heads, "d_k": sh.d_k,
+                "d_v": sh.d_v, "grid_c": sh.grid_c, "inputs": "bf16", "state": "fp32", "outputs": "fp32",
+                "l2": "inputs larger than L2", "parallelism": "replicas"}
+
+
+class LongStep:
+    """One 100,000-token session (Hk 16, Hv 32, slow decay) in 6 turns, each writing its checkpoint, then
+    64 forks of 20..200 question tokens over the committed state. The forks run as one branches call:
+    each branch is the pending tail plus its question, starting from the committed state read in place
+    (so the state needs no restore afterwards)."""
+
+    def __init__(self, w, device):
+        import torch
+        from chunked_gated_deltanet_gb300 import gdn
+        from chunked_gated_deltanet_gb300 import workloads as wl
+        self.gdn, self.w = gdn, w
+        sh = w.shape
+        C = sh.grid_c
+        self.desc = gdn.make_desc(sh.n_qk_heads, sh.n_v_heads, sh.d_k, sh.d_v, sh.grid_c, gdn.GDN_BF16, gdn.GDN_FP32)
+        T = w.session_lengths[0]
+        tok = w.session_tokens(0)
+        self.x = wl.tokens_to_torch(tok, sh.dtype, device)
+        self.out = torch.empty((T, sh.n_v_heads, sh.d_v), dtype=torch.float32, device=device)
+        self.calls, end, committed = [], 0, 0
+        for n in w.turns[0]:
+            end += n
+            take = (end - committed) // C * C
+            self.calls.append((committed, end, take))
+            committed += take
+        tail = tok.slice(committed, T)
+        forks = [wl.Tokens.concat([tail, w.extra_tokens(j, q)]) for j, q in enumerate(w.fork_questions)]
+        self.cu = [0]
+        for f in forks:
+            self.cu.append(self.cu[-1] + len(f))
+        self.xf = wl.tokens_to_torch(wl.Tokens.concat(forks), sh.dtype, device)
+        self.outf = torch.empty((self.cu[-1], sh.n_v_heads, sh.d_v), dtype=torch.float32, device=device)
+        self.cw = wl.to_torch(w.conv_weights(), sh.dtype, device)
+        max_call = max([e - s for s, e, _ in self.calls] + [self.cu[-1]])
+        self.ws = gdn.workspace(self.desc, max_call + 64 * len(forks), len(forks), device)
+        self.sess = gdn.Session(self.desc, device)
+        self.slots = [gdn.Session(self.desc, device) for _ in range(w.n_slots)]
+        self.branches = [gdn.Session(self.desc, device) for _ in forks]
+        self.committed, self.n_forks = committed, len(forks)
+        self.tokens_per_step = committed + self.cu[-1]
+        self.block_steps_per_step = sum(-(-t // 64) for _, _, t in self.calls) + max(-(-len(f) // 64) for f in forks)
+
+    def step(self):
+        g, d, x, cw = self.gdn, self.desc, self.x, self.cw
+        g.gdn_session_init(d, self.sess)
+        for k, (a, b, take) in enumerate(self.calls):
+            n = g.gdn_prefill_chunks_checkpoint(d, self.sess, self.slots[k % len(self.slots)], *(t[a:b] for t in x), cw,
+                                                self.out[a:b], self.ws)
+            assert n == take
+        g.gdn_prefill_branches(d, self.sess, self.branches, self.cu, *self.xf, cw, self.outf, self.ws,
+                               flags=g.GDN_ALLOW_PARTIAL)
+
+    def config(self):
+        sh = self.w.shape
+        return {"workload": self.w.name, "sessions": 1, "session_tokens": self.w.session_lengths[0],
+                "turns": len(self.calls), "checkpoint_slots": len(self.slots), "forks": self.n_forks,
+                "fork_tokens": self.cu[-1], "forks_as": "one branches call from the committed state",
+                "tokens_per_step": self.tokens_per_step, "n_qk_heads": sh.n_qk_heads, "n_v_heads": sh.n_v_heads,
+                "d_k": sh.d_k, "d_v": sh.d_v, "grid_c": sh.grid_c, "inputs": "bf16", "state": "fp32",
+                "outputs": "fp32", "l2": "inputs larger than L2", "parallelism": "replicas"}
 
 
 # ---------------------------------------------------------------------------
@@ -480,13 +628,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode and branch measurements")
     ap.add_argument("--cpu-sample-tokens", type=int, default=41472)
+    ap.add_argument("--workload", choices=["replay", "varlen8", "long_session"], default="replay",
+                    help="replay: the headline (default); varlen8 / long_session: the batch and long-session "
+                         "configurations, reported without e2e")
     args = ap.parse_args()
     if args.warmup < 3:
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
 
     rank, world, local = _dist()
     from chunked_gated_deltanet_gb300 import workloads as wl
-    w = wl.qwen08b_replay()
+    w = {"replay": wl.qwen08b_replay, "varlen8": wl.varlen8, "long_session": wl.long_session}[args.workload]()
 
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
@@ -496,7 +647,9 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     gdn.load_library()
-    step = ReplayStep(w, dev)
+    step = {"replay": ReplayStep, "varlen8": VarlenStep, "long_session": LongStep}[args.workload](w, dev)
+    if args.workload != "replay":   # the e2e, decode and branch figures belong to the headline workload
+        args.no_e2e = args.no_decode = True
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -562,7 +715,7 @@ def main():
     tokens_per_launch = step.tokens_per_step / prefill_launches
     achieved = bpt * tokens_per_launch / (avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peaks()
-    traffic_bpt = traffic_record(name)
+    traffic_bpt = traffic_record(name) if args.workload == "replay" else None   # profiled on the replay
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_src, "kernel": name,
                 "algorithmic_bytes_per_token": bpt, "tokens_per_launch": round(tokens_per_launch, 1),
@@ -571,6 +724,21 @@ def main():
                 "step_frac": round(bpt * step.tokens_per_step / (ms / args.steps / 1e3) / 1e9 / peak, 4)}
     kernels = {k: {"launches_per_step": v[0] / args.steps, "ms_per_step": round(v[2] / args.steps, 4),
                    "share": round(v[2] / sum(x[2] for x in ktimes.values()), 4)} for k, v in ktimes.items()}
+    # the state pass: tensor-pipe fraction against the tf32 rate measured now, and the single-session latency
+    # floor (dependent 64-token block steps of one head x the measured time per step)
+    state_pass = None
+    if "state_output" in ktimes:
+        launches, timed, tot = ktimes["state_output"]
+        blocks = step.block_steps_per_step * args.steps
+        us_block = tot * 1e3 / blocks
+        flops = 6.0 * sh.d_k * sh.d_v * sh.n_v_heads * step.tokens_per_step * args.steps
+        tf32 = tf32_tflops_probe(dev)
+        achieved_tf = flops / (tot / 1e3) / 1e12
+        state_pass = {"bound": "latency", "us_per_block_step": round(us_block, 3),
+                      "latency_floor_ms_per_step": round(step.block_steps_per_step * us_block / 1e3, 3),
+                      "tensor": {"flops_per_token": 6 * sh.d_k * sh.d_v * sh.n_v_heads, "achieved_tflops":
+                                 round(achieved_tf, 1), "tf32_tflops_measured_now": round(tf32, 1),
+                                 "frac": round(achieved_tf / tf32, 4)}}
     gpu_launches = int(sum(v[0] for v in ktimes.values()))
 
     decode = None if args.no_decode else [decode_measure(w, dev, n) for n in (1, 64)]
@@ -580,7 +748,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": step.config(),
             "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline, "kernels": kernels, "clocks": clocks,
-            "decode": decode, "branches": branches}
+            "state_pass": state_pass, "decode": decode, "branches": branches}
 
     # --- CPU baseline (oracle), rank 0 at N=1 only ---
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -590,7 +758,7 @@ def main():
         run()
         dt = time.time() - t0
         line["cpu_baseline"] = {"value": round(n / dt, 1), "unit": UNIT, "cores": cpu_threads(sh.n_v_heads),
-                                "kind": "oracle",
+                                "kind": "oracle", "cpu": cpu_model(),
                                 "sample": f"first {n} tokens of the {w.session_lengths[0]}-token session, all "
                                           f"{sh.n_v_heads} heads, one fp64 oracle call ({dt:.1f} s)"}
     if rank == 0:
