@@ -21,19 +21,40 @@ __device__ unsigned int g_gdn_device_error;
 
 namespace gdn {
 
-template <int D>
+// Shared-memory plan of a CTA with DS state columns. With 16 columns both operand sets of a block (A of
+// the first product, [W; Qe], and of the second, K_tilde^T, with the U and O_intra slices) are double
+// buffered. With 32 columns that does not fit: the K_tilde^T part stays double buffered and [W; Qe] has
+// one buffer, refilled for the next block while the second product runs.
+template <int D, int DS>
+struct ChainPlan {
+    static constexpr bool kSplit = DS > kSliceCols;
+    static constexpr int SP = DS + 8;          // tf32 S^T and U' rows (B fragments): banks 8t + g, distinct
+    static constexpr int WQF = 2 * kBlock * D; // [W; Qe] fragments
+    static constexpr int KTF = kBlock * D;     // K_tilde^T fragments
+    static constexpr int UF = kBlock * DS;     // U (or O_intra) fragments of the CTA's columns
+    static constexpr int KSTAGE = KTF + 2 * UF + 4;                        // K_tilde^T, U, O_intra, e^{gamma_63}
+    static constexpr int STAGE = kSplit ? KSTAGE : WQF + KSTAGE;           // one double-buffered stage
+    static constexpr int WQBUF = kSplit ? WQF : 0;                         // the single [W; Qe] buffer
+    static constexpr size_t bytes() {
+        return sizeof(float) * (2 * STAGE + WQBUF + D * SP + kBlock * SP) + 4 * sizeof(uint64_t);
+    }
+};
+
+template <int D, int DS>
 __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommon p, int64_t ch) {
     extern __shared__ __align__(16) float smem[];
-    constexpr int DS = kSliceCols, NT = DS / 8;
-    constexpr int SP = DS + 8;                 // tf32 S^T and U' rows (B fragments): banks 24t + g, distinct
-    constexpr int WQF = 2 * kBlock * D;        // [W; Qe] fragments
-    constexpr int KTF = kBlock * D;            // K_tilde^T fragments
-    constexpr int UF = kBlock * DS;            // one slice of U (or O_intra) fragments
-    constexpr int STAGE = WQF + KTF + 2 * UF + 4;
+    using P = ChainPlan<D, DS>;
+    constexpr int NT = DS / 8, SP = P::SP, WQF = P::WQF, KTF = P::KTF, UF = P::UF, STAGE = P::STAGE;
+    constexpr bool kSplit = P::kSplit;
     static_assert(D == 128 || D == 64, "head dim");
-    float *St = smem + 2 * STAGE;              // [D][SP]   tf32 copy of the state slice
+    static_assert(DS == 16 || DS == 32, "slice width");
+    float *wqbuf = smem + 2 * STAGE;           // [W; Qe] of the current block (split plan only)
+    float *St = wqbuf + P::WQBUF;              // [D][SP]   tf32 copy of the state slice
     float *Ups = St + D * SP;                  // [64][SP]  tf32 U'
-    uint64_t *bar = reinterpret_cast<uint64_t *>(Ups + kBlock * SP);   // [2] stage barriers
+    uint64_t *bar = reinterpret_cast<uint64_t *>(Ups + kBlock * SP);   // [0..1] stages, [2] [W; Qe] buffer
+    // block b's operands: A of the first product, then K_tilde^T, U, O_intra, e^{gamma_63}
+    auto wq_of = [&](int b) -> const float * { return kSplit ? wqbuf : smem + (b & 1) * STAGE; };
+    auto kt_of = [&](int b) -> const float * { return smem + (b & 1) * STAGE + (kSplit ? 0 : WQF); };
 
     constexpr int nsl = D / DS;
     const int sl = blockIdx.x % nsl;
@@ -77,21 +98,32 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
         }
     }
 
-    // block b's operands -> stage b & 1 (thread 0 only)
+    // block b's operands -> stage b & 1 (thread 0 only): with the 16-column plan all of them, with the
+    // split plan the K_tilde^T part ([W; Qe] goes through issue_wq)
+    constexpr int CHUNK = 4096;   // floats per bulk copy (16 KB)
+    static_assert(WQF % CHUNK == 0 && KTF % CHUNK == 0, "operand blocks are whole numbers of chunks");
     auto issue = [&](int b) {
         float *buf = smem + (b & 1) * STAGE;
         const float *r = p.ws_wu + ((int64_t)(s.blk0 + b) * Hv + h) * RF;
         uint64_t *br = &bar[b & 1];
         if (b == 0 && p.debug_skip_first_copy == 1) return;   // test hook: leave the barrier pending
         fence_proxy_async();
-        mbar_arrive_expect_tx(br, (uint32_t)sizeof(float) * (WQF + KTF + 2 * UF + 4));
-        constexpr int CHUNK = 4096;   // floats per bulk copy (16 KB)
-        static_assert((WQF + KTF) % CHUNK == 0, "operand block is a whole number of chunks");
+        mbar_arrive_expect_tx(br, (uint32_t)sizeof(float) * STAGE);
+        const int first = kSplit ? WQF / CHUNK : 0;           // the split plan skips [W; Qe]
 #pragma unroll
-        for (int q = 0; q < (WQF + KTF) / CHUNK; ++q) bulk_g2s(buf + q * CHUNK, r + q * CHUNK, sizeof(float) * CHUNK, br);
-        bulk_g2s(buf + WQF + KTF, r + 192 * D + sl * UF, sizeof(float) * UF, br);
-        bulk_g2s(buf + WQF + KTF + UF, r + 256 * D + sl * UF, sizeof(float) * UF, br);
-        bulk_g2s(buf + WQF + KTF + 2 * UF, r + 320 * D, 16, br);
+        for (int q = first; q < (WQF + KTF) / CHUNK; ++q)
+            bulk_g2s(buf + (q - first) * CHUNK, r + q * CHUNK, sizeof(float) * CHUNK, br);
+        float *u = buf + STAGE - 2 * UF - 4;
+        bulk_g2s(u, r + 192 * D + sl * UF, sizeof(float) * UF, br);
+        bulk_g2s(u + UF, r + 256 * D + sl * UF, sizeof(float) * UF, br);
+        bulk_g2s(u + 2 * UF, r + 320 * D, 16, br);
+    };
+    auto issue_wq = [&](int b) {   // split plan: [W; Qe] of block b into its single buffer
+        const float *r = p.ws_wu + ((int64_t)(s.blk0 + b) * Hv + h) * RF;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&bar[2], (uint32_t)sizeof(float) * WQF);
+#pragma unroll
+        for (int q = 0; q < WQF / CHUNK; ++q) bulk_g2s(wqbuf + q * CHUNK, r + q * CHUNK, sizeof(float) * CHUNK, &bar[2]);
     };
 
     // state rows in registers (fp32), tf32 copy in shared memory
@@ -117,17 +149,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
     if (t == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        mbar_init(&bar[2], 1);
         mbar_init_fence();
     }
     __syncthreads();
-    if (t == 0 && nb > 0) issue(0);
+    if (t == 0 && nb > 0) {
+        issue(0);
+        if constexpr (kSplit) issue_wq(0);
+    }
 
     int timed_out = 0;
     for (int b = 0; b < nb; ++b) {
-        const float *buf = smem + (b & 1) * STAGE;
+        const float *wq = wq_of(b), *kt = kt_of(b), *uo0 = kt + KTF;
         if (t == 0 && b + 1 < nb) issue(b + 1);   // the other stage was released at the end of step b-1
         // every thread acquires the stage itself; a timeout is acted on at the end of the step
         if (!mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit)) timed_out = b + 1;
+        if constexpr (kSplit)
+            if (!mbar_wait_bounded(&bar[2], b & 1, p.wait_limit)) timed_out = b + 1;
 
         // Z = [W; Qe] S^T, four partial accumulators per n-tile (k-step mod 4)
         float acc[4][NT][4];
@@ -138,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
 #pragma unroll
                 for (int f = 0; f < 4; ++f) acc[j][nt][f] = 0.f;
         {
-            const float4 *wa = reinterpret_cast<const float4 *>(buf) + (warp * (D / 8)) * 32 + lane;
+            const float4 *wa = reinterpret_cast<const float4 *>(wq) + (warp * (D / 8)) * 32 + lane;
 #pragma unroll
             for (int ks = 0; ks < D / 8; ++ks) {
                 const float4 av = wa[ks * 32];
@@ -157,10 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
         {
             const int nrow = min(kBlock, s.n - b * kBlock);
             const int w4 = warp & 3;
-            const float4 *uo = reinterpret_cast<const float4 *>(buf + WQF + KTF + (warp < 4 ? 0 : UF));
+            const float4 *uo = reinterpret_cast<const float4 *>(uo0 + (warp < 4 ? 0 : UF));
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const float4 u = uo[(w4 * NT + nt) * 32 + lane];
+                // fragments are stored by 16-column slice: [slice][m-tile][n-tile of 8][lane][4]
+                const float4 u = uo[(((nt >> 1) * 4 + w4) * 2 + (nt & 1)) * 32 + lane];
                 float z[4];
 #pragma unroll
                 for (int f = 0; f < 4; ++f) z[f] = (acc[0][nt][f] + acc[1][nt][f]) + (acc[2][nt][f] + acc[3][nt][f]);
@@ -186,10 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
                 }
             }
         }
-        __syncthreads();  // (B) U' complete; every read of the tf32 state copy done
+        __syncthreads();  // (B) U' complete; every read of the tf32 state copy and of [W; Qe] done
+        if constexpr (kSplit)
+            if (t == 0 && b + 1 < nb) issue_wq(b + 1);   // refilled while the second product runs
         // S^T <- e^{gamma_63} S^T + K_tilde^T U' on the owner warps' registers
         if (owner) {
-            const float e = buf[WQF + KTF + 2 * UF];
+            const float e = uo0[2 * UF];
             float cx[3][NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -198,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
                     st[nt][f] *= e;
                     cx[0][nt][f] = cx[1][nt][f] = cx[2][nt][f] = 0.f;
                 }
-            const float4 *ka = reinterpret_cast<const float4 *>(buf + WQF) + (warp * 8) * 32 + lane;
+            const float4 *ka = reinterpret_cast<const float4 *>(kt) + (warp * 8) * 32 + lane;
 #pragma unroll
             for (int ks = 0; ks < kBlock / 8; ++ks) {
                 const float4 av = ka[ks * 32];
@@ -237,6 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
             const int b = timed_out - 1;
             if (!(b == 0 && p.debug_skip_first_copy == 1)) mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
             if (b + 1 < nb) mbar_wait_bounded(&bar[(b + 1) & 1], ((b + 1) >> 1) & 1, p.wait_limit);
+            if constexpr (kSplit) {   // [W; Qe] of block b (if its wait ran out) and of block b + 1
+                mbar_wait_bounded(&bar[2], b & 1, p.wait_limit);
+                if (b + 1 < nb) mbar_wait_bounded(&bar[2], (b + 1) & 1, p.wait_limit);
+            }
         }
         __syncthreads();
         return;
@@ -260,22 +305,36 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const LaunchCommo
     }
 }
 
-template <int D>
+template <int D, int DS>
 static cudaError_t launch(const LaunchCommon &p, int64_t ch, cudaStream_t st) {
-    constexpr int DS = kSliceCols, SP = DS + 8;
-    constexpr size_t smem = sizeof(float) * (2 * (2 * kBlock * D + kBlock * D + 2 * kBlock * DS + 4) + D * SP +
-                                             kBlock * SP) + 2 * sizeof(uint64_t);
-    auto k = chain_tc_kernel<D>;
+    constexpr size_t smem = ChainPlan<D, DS>::bytes();
+    static_assert(smem <= 227 * 1024, "shared memory");
+    auto k = chain_tc_kernel<D, DS>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     k<<<p.n_sess * p.Hv * (D / DS), kThreads, smem, st>>>(p, ch);
     return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_d(const LaunchCommon &p, int64_t ch, cudaStream_t st) {
+    // 16 columns per CTA while the launch fits one wave (one CTA per SM): the shortest step for a few
+    // chains; 32 columns once it would not, where throughput counts. The arithmetic of every state
+    // element is the same in both (same MMAs, same accumulation order), so results do not depend on it.
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 1;
+    }
+    if ((int64_t)p.n_sess * p.Hv * (D / kSliceCols) > sms) return launch<D, 2 * kSliceCols>(p, ch, st);
+    return launch<D, kSliceCols>(p, ch, st);
+}
+
 }  // namespace gdn
 
 cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st) {
-    return D == 64 ? gdn::launch<64>(p, ch, st) : gdn::launch<128>(p, ch, st);
+    return D == 64 ? gdn::launch_d<64>(p, ch, st) : gdn::launch_d<128>(p, ch, st);
 }
 
 #include <mutex>
