@@ -163,3 +163,46 @@ def test_state_call_refusals(lib):
 def test_status_strings(lib):
     assert lib.gdn_status_string(gdn.GDN_ERR_OFF_GRID) == b"GDN_ERR_OFF_GRID"
     assert lib.gdn_status_string(99) == b"unknown status"
+
+
+def _fake(desc, base, committed=0):
+    # device addresses that are never dereferenced: every call below is refused first
+    return gdn.gdn_session(ctypes.c_void_p(base), ctypes.c_void_p(base + 0x100000), committed, gdn.gdn_desc_tag(desc))
+
+
+def test_branch_and_checkpoint_refusals(lib):
+    d = _desc(grid_c=64)
+    vp = ctypes.c_void_p
+    x = [vp(0x7000000 + 0x10000 * i) for i in range(7)]     # xq, xk, xv, g, beta, conv_w, out
+    cu = (ctypes.c_int64 * 3)(0, 64, 128)
+    nc = (ctypes.c_int64 * 2)()
+    prefix = _fake(d, 0x1000000, committed=128)
+    br = (gdn.gdn_session * 2)(_fake(d, 0x2000000), _fake(d, 0x3000000))
+
+    def branches(pref, arr, flags=0):
+        return lib.gdn_prefill_branches(ctypes.byref(d), pref, arr, 2, cu, *x[:6], flags, x[6], nc,
+                                        vp(0x9000000), 1 << 30, None)
+
+    assert branches(None, br) == gdn.GDN_ERR_INVALID_ARG
+    alias = (gdn.gdn_session * 2)(_fake(d, 0x2000000), _fake(d, 0x1000000))   # a branch is the prefix
+    assert branches(ctypes.byref(prefix), alias) == gdn.GDN_ERR_INVALID_ARG
+    off = _fake(d, 0x1000000, committed=100)                                 # off grid, no partial flag
+    assert branches(ctypes.byref(off), br) == gdn.GDN_ERR_OFF_GRID
+    foreign = _fake(_desc(grid_c=128), 0x1000000, committed=128)
+    assert branches(ctypes.byref(foreign), br) == gdn.GDN_ERR_STATE_MISMATCH
+    assert [b.committed for b in br] == [0, 0] and prefix.committed == 128
+
+    s = _fake(d, 0x4000000)
+    slot = _fake(d, 0x5000000, committed=-1)
+
+    def ckpt(sess, sl):
+        return lib.gdn_prefill_chunks_checkpoint(ctypes.byref(d), ctypes.byref(sess), ctypes.byref(sl), *x[:6], 64,
+                                                 0, x[6], ctypes.byref(ctypes.c_int64()), vp(0x9000000), 1 << 30,
+                                                 None)
+
+    assert ckpt(s, _fake(d, 0x4000000)) == gdn.GDN_ERR_INVALID_ARG           # the slot is the session
+    nul = gdn.gdn_session(None, None, -1, gdn.gdn_desc_tag(d))
+    assert ckpt(s, nul) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_prefill_varlen_checkpoint(ctypes.byref(d), ctypes.byref(s), None, 1, cu, *x[:6], 0, x[6], nc,
+                                             vp(0x9000000), 1 << 30, None) == gdn.GDN_ERR_INVALID_ARG
+    assert (slot.committed, s.committed) == (-1, 0)
