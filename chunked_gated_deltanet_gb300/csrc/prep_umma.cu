@@ -58,6 +58,7 @@ constexpr uint32_t OFF_W = OFF_SMALL + 4 * 3 * kBlock;       // q, k, v conv wei
 constexpr uint32_t OFF_BAR = OFF_W + 3 * W_BYTES;            // [0] input copies, [1] MMA groups; TMEM slot
 constexpr uint32_t SMEM = OFF_BAR + 32;
 constexpr uint32_t RAW_ROW = 2 * D, RAW_TILE = (kBlock + 3) * RAW_ROW;
+constexpr uint32_t TILE_BYTES = RAW_TILE + W_BYTES;           // one staged tile: 64 + 3 rows and its weights
 constexpr uint32_t OFF_RAW = OFF_PH;                         // raw input tiles: dead before P, T, A are written
 static_assert(OFF_RAW + 3 * RAW_TILE <= OFF_SMALL, "raw tiles must fit the P, T and inverse regions");
 static_assert(OFF_ATL + 2 * R64_BYTES <= OFF_MT, "[T; P T] must fit over A and T");
@@ -182,16 +183,27 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     __nv_bfloat16 *rawk = rawq + (kBlock + 3) * D, *rawv = rawk + (kBlock + 3) * D;
     __nv_bfloat16 *wq = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W), *wk = wq + 4 * D, *wv = wk + 4 * D;
 
-    const int blk = blockIdx.x, hk = blockIdx.y, t = threadIdx.x;
-    const int warp = t >> 5, lane = t & 31;
-    const SessRef s = p.s[find_session(p, blk)];
-    const int pos0 = (blk - s.blk0) * kBlock;
-    const int n = min(kBlock, s.n - pos0);
-    const int64_t row0 = s.row0 + pos0;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int Hk = p.Hk, Hv = p.Hv;
     const int64_t nq = (int64_t)Hk * D, nv = (int64_t)Hv * D;
     const __nv_bfloat16 *cw = static_cast<const __nv_bfloat16 *>(p.conv_w);
-    const __nv_bfloat16 *cs = static_cast<const __nv_bfloat16 *>(s.conv0);
+    // A task is one (64-token block, q/k head); a CTA takes tasks blockIdx.x, + gridDim.x, ... (one CTA per
+    // SM), and stages the next task's inputs during the current task's record epilogue.
+    struct Task { int blk, hk, pos0, n; int64_t row0; SessRef s; };
+    auto task_of = [&](int tau) {
+        Task k;
+        k.blk = tau % p.nblk;
+        k.hk = tau / p.nblk;
+        k.s = p.s[find_session(p, k.blk)];
+        k.pos0 = (k.blk - k.s.blk0) * kBlock;
+        k.n = min(kBlock, k.s.n - k.pos0);
+        k.row0 = k.s.row0 + k.pos0;
+        return k;
+    };
+    const int ntask = p.nblk * Hk;
+    int tau = blockIdx.x;
+    Task cur = task_of(tau), nxt = cur;
+    int blk = cur.blk, hk = cur.hk, n = cur.n;
 
     if (warp == 0) {
         tmem_alloc(tslot, 512);
@@ -209,37 +221,42 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     uint32_t in_phase = 0, mma_phase = 0;
     int in_pending = 0, mma_pending = 0;   // an issued copy group / MMA group not yet seen complete (CTA-uniform)
 
-    // Stage rows pos0-3 .. pos0+63 of `ntile` head tiles and their conv weights: one tensor copy of the
-    // block's 64 rows per tile (rows past the inputs read as zero, rows past n belong to other tokens and
-    // only reach masked results); the three halo rows (from the inputs or, before a call's first token,
-    // from the conv state) and the weights by plain 16-byte loads of warps 1-15.
+    // Stage rows pos0-3 .. pos0+63 of task k's q and k tiles (with_qk) and of v-head h's v tile, with their
+    // conv weights: one tensor copy of the block's 64 rows per tile (rows past the inputs read as zero, rows
+    // past n belong to other tokens and only reach masked results), issued by thread 0 with the byte count;
+    // the three halo rows (from the inputs or, before a call's first token, from the conv state) and the
+    // weights as single bulk copies, one per warp 1.., so that no warp waits on them.
     struct Tile { __nv_bfloat16 *dst, *wdst; const CUtensorMap *map; const __nv_bfloat16 *x; int64_t ld, col0, chan0; };
-    auto stage = [&](const Tile *tl, int ntile, bool skip) {
+    auto tile_of = [&](int q, const Task &k, int h) -> Tile {
+        if (q == 0) return {rawq, wq, &p.tm_q, static_cast<const __nv_bfloat16 *>(p.xq), nq, (int64_t)k.hk * D, (int64_t)k.hk * D};
+        if (q == 1)
+            return {rawk, wk, &p.tm_k, static_cast<const __nv_bfloat16 *>(p.xk), nq, (int64_t)k.hk * D, nq + (int64_t)k.hk * D};
+        return {rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)h * D, 2 * nq + (int64_t)h * D};
+    };
+    auto stage = [&](const Task &k, int h, bool with_qk, bool skip) {
         in_pending = 1;
         if (skip) return;
-        constexpr int HALO = 3 * (D / 8), WCH = W_BYTES / 16, PER = HALO + WCH;   // 16-byte chunks per tile
-        if (warp == 0) {
-            if (lane == 0) mbar_arrive_expect_tx(&bar[0], (uint32_t)ntile * kBlock * RAW_ROW);
-            __syncwarp();
-#pragma unroll
-            for (int q = 0; q < 3; ++q)
-                if (q < ntile && lane == q) tma_load_2d(tl[q].dst + 3 * D, tl[q].map, (int)tl[q].col0, (int)row0, &bar[0]);
-        } else {
-            const int e = t - 32;
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-                if (q >= ntile || e < PER * q || e >= PER * (q + 1)) continue;
-                const int k = e - PER * q;
-                if (k < HALO) {
-                    const int r = k / (D / 8), c = (k % (D / 8)) * 8, pos = pos0 - 3 + r;
-                    const __nv_bfloat16 *src =
-                        pos < 0 ? cs + (int64_t)(3 + pos) * ch + tl[q].chan0 : tl[q].x + (s.row0 + pos) * tl[q].ld + tl[q].col0;
-                    *reinterpret_cast<uint4 *>(tl[q].dst + r * D + c) = __ldg(reinterpret_cast<const uint4 *>(src + c));
-                } else {
-                    const int kw = k - HALO;
-                    *reinterpret_cast<uint4 *>(tl[q].wdst + kw * 8) =
-                        __ldg(reinterpret_cast<const uint4 *>(cw + tl[q].chan0 * 4 + kw * 8));
-                }
+        const int q0 = with_qk ? 0 : 2, ntile = 3 - q0;
+        // the region was last written by generic stores (ordered by the barriers since): order them
+        // before the async-proxy writes of the copies
+        if (t == 0 || (lane == 0 && warp >= 1 && warp <= 4 * ntile)) fence_proxy_async();
+        if (t == 0) {
+            mbar_arrive_expect_tx(&bar[0], (uint32_t)ntile * TILE_BYTES);
+            for (int q = q0; q < 3; ++q) {
+                const Tile tl = tile_of(q, k, h);
+                tma_load_2d(tl.dst + 3 * D, tl.map, (int)tl.col0, (int)k.row0, &bar[0]);
+            }
+        }
+        if (lane == 0 && warp >= 1 && warp <= 4 * ntile) {
+            const int e = warp - 1, r = e & 3;
+            const Tile tl = tile_of(q0 + (e >> 2), k, h);
+            if (r < 3) {
+                const int pos = k.pos0 - 3 + r;
+                const __nv_bfloat16 *src = pos < 0 ? static_cast<const __nv_bfloat16 *>(k.s.conv0) + (int64_t)(3 + pos) * ch + tl.chan0
+                                                   : tl.x + (k.s.row0 + pos) * tl.ld + tl.col0;
+                bulk_g2s(tl.dst + r * D, src, RAW_ROW, &bar[0]);
+            } else {
+                bulk_g2s(tl.wdst, cw + tl.chan0 * 4, W_BYTES, &bar[0]);
             }
         }
     };
@@ -338,23 +355,25 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
         });
     };
 
-    {   // 1. q, k and the first v-head's tiles
-        const Tile tl[3] = {
-            {rawq, wq, &p.tm_q, static_cast<const __nv_bfloat16 *>(p.xq), nq, (int64_t)hk * D, (int64_t)hk * D},
-            {rawk, wk, &p.tm_k, static_cast<const __nv_bfloat16 *>(p.xk), nq, (int64_t)hk * D, nq + (int64_t)hk * D},
-            {rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)(hk * p.G) * D, 2 * nq + (int64_t)(hk * p.G) * D}};
-        stage(tl, 3, p.debug_skip_first_copy == 2);
-    }
-    // gamma (inclusive scan of g over the block), beta and e^gamma of v-head h, by warps 2 and 3 alone while
-    // the input copies are in flight: warp 3 adds the total of rows 0..31 itself, so no barrier is needed
+    stage(cur, hk * p.G, true, p.debug_skip_first_copy == 2);   // 1. the first task's tiles
+    // gamma (inclusive scan of g over the block), beta and e^gamma of v-head h, by warps 2 and 3 alone: warp 3
+    // adds the total of rows 0..31 itself, so no barrier is needed. The loads can be issued early (for the
+    // next task, during the current one's record epilogue) and the scan run later.
     const int jg = t - 64;
-    auto gates = [&](int h) {
+    struct Gv { float g, b, lo; };
+    auto gates_load = [&](const Task &k, int h) {
+        Gv r{0.f, 0.f, 0.f};
+        if (jg < 0 || jg >= kBlock) return r;
+        if (jg < k.n) {
+            r.g = p.g[(k.row0 + jg) * Hv + h];
+            r.b = p.beta[(k.row0 + jg) * Hv + h];
+        }
+        if (jg >= 32 && lane < k.n) r.lo = p.g[(k.row0 + lane) * Hv + h];
+        return r;
+    };
+    auto gates_store = [&](Gv r) {
         if (jg < 0 || jg >= kBlock) return;
-        const float gv = jg < n ? p.g[(row0 + jg) * Hv + h] : 0.f;
-        const float bv = jg < n ? p.beta[(row0 + jg) * Hv + h] : 0.f;
-        float lo = 0.f;
-        if (jg >= 32 && lane < n) lo = p.g[(row0 + lane) * Hv + h];
-        float sv = gv;
+        float sv = r.g, lo = r.lo;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, sv, o);
@@ -366,11 +385,14 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
             sv += lo;
         }
         gam[jg] = sv;
-        bet[jg] = bv;
+        bet[jg] = r.b;
         egv[jg] = expf(sv);
     };
-    gates(hk * p.G);
-    bool ok = wait_in();
+    gates_store(gates_load(cur, hk * p.G));
+    Gv gnext{0.f, 0.f, 0.f};
+    bool ok = true;
+    for (;;) {   // tasks
+    ok = wait_in();
 
     if (ok) {
         // 2. conv + L2 norm of q (warps 0-7) and k (warps 8-15), 8 rows per warp -> bf16 hi/lo rows of [q_hat; k_hat]
@@ -414,9 +436,8 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     for (int gi = 0; ok && gi < p.G; ++gi) {
         const int h = hk * p.G + gi;
         if (gi > 0) {   // the previous head is done with the raw-tile region and every MMA operand
-            const Tile tl[1] = {{rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)h * D, 2 * nq + (int64_t)h * D}};
-            stage(tl, 1, false);
-            gates(h);
+            stage(cur, h, false, false);
+            gates_store(gates_load(cur, h));
             if (!(ok = wait_in())) break;
         }
         float *rec = p.ws_wu + ((int64_t)blk * Hv + h) * rec_floats(D);
@@ -600,6 +621,12 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
         kt_record(1);
         if (!(ok = wait_mma())) break;
 
+        // the next task's inputs: the raw-tile region and the weights are free from here on
+        if (gi == p.G - 1 && tau + (int)gridDim.x < ntask) {
+            nxt = task_of(tau + gridDim.x);
+            stage(nxt, nxt.hk * p.G, true, false);
+            gnext = gates_load(nxt, nxt.hk * p.G);
+        }
         // 11. the record, every warp (lanes 32 (warp % 4) .., 64 columns at 64 (warp / 4)):
         //     W rows -> tf32 A fragments (rows 0..63 of [W; Qe]); U rows -> C fragments;
         //     P W rows -> Qe = e^gamma q_hat - P W (rows 64..127 of [W; Qe]); P U rows -> O_intra C fragments
@@ -637,6 +664,13 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
         tc_fence_before();
         __syncthreads();   // TMEM columns and every operand region are free for the next v-head
     }
+    if (!ok) break;
+    tau += gridDim.x;
+    if (tau >= ntask) break;
+    cur = nxt;
+    blk = cur.blk; hk = cur.hk; n = cur.n;
+    gates_store(gnext);
+    }   // tasks
 
     if (!ok) {   // a bounded wait ran out: record it and wait (bounded) for what is still in flight
         if (t == 0) {
@@ -657,6 +691,13 @@ cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStr
     using namespace gdn;
     cudaError_t e = cudaFuncSetAttribute(prep_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)up::SMEM);
     if (e != cudaSuccess) return e;
-    prep_umma_kernel<<<dim3(p.nblk, p.Hk), kUmmaPrepThreads, up::SMEM, st>>>(p, ch);
+    static int sms = 0;   // one persistent CTA per SM (shared memory allows no more), over nblk x Hk tasks
+    if (!sms) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 1;
+    }
+    const int ntask = p.nblk * p.Hk;
+    prep_umma_kernel<<<ntask < sms ? ntask : sms, kUmmaPrepThreads, up::SMEM, st>>>(p, ch);
     return cudaGetLastError();
 }
