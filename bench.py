@@ -462,6 +462,9 @@ class LongStep:
 # Batched decode (one token for each of n sessions), captured once in a CUDA graph
 # ---------------------------------------------------------------------------
 
+L2_BYTES = 129 * 1024 * 1024
+
+
 def decode_measure(w, dev, n_sess: int = 64, steps: int = 50):
     """Replays of one captured decode step over n_sess sessions of the bench layer; HBM roofline of the
     step = every state read and written once, plus the conv states, inputs and outputs."""
@@ -498,7 +501,8 @@ def decode_measure(w, dev, n_sess: int = 64, steps: int = 50):
     bytes_step = 2 * state + 2 * conv + io
     peak, _ = measured_peaks()
     gbs = bytes_step / (us / 1e6) / 1e9
-    return {"sessions": n_sess, "launch": "CUDA graph replay of one gdn_decode_step", "us_per_step": round(us, 2),
+    l2 = "state larger than L2" if state > L2_BYTES else "state fits L2 (replays may hit it)"
+    return {"sessions": n_sess, "launch": "CUDA graph replay of one gdn_decode_step", "l2": l2, "us_per_step": round(us, 2),
             "tokens_per_s": round(n_sess / (us / 1e6), 1), "bytes_per_step": bytes_step,
             "achieved_gbs": round(gbs, 1), "peak_gbs": peak, "frac": round(gbs / peak, 4), "bound": "hbm"}
 
@@ -741,7 +745,7 @@ def main():
                                  "frac": round(achieved_tf / tf32, 4)}}
     gpu_launches = int(sum(v[0] for v in ktimes.values()))
 
-    decode = None if args.no_decode else [decode_measure(w, dev, n) for n in (1, 64)]
+    decode = None if args.no_decode else [decode_measure(w, dev, n) for n in (1, 64, 256)]
     branches = None if args.no_decode else branches_measure(dev)
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -580,8 +580,6 @@ GDN_API gdn_status gdn_decode_step(const gdn_layer_desc *d, gdn_session *session
         cudaStream_t cst = (cudaStream_t)stream;
         cudaError_t e = launch_k(K_DECODE, cst, [&] { return gdn_launch_decode(p, D, in_bf16, ch, cst); });
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
-        e = launch_k(K_CONV, cst, [&] { return gdn_launch_conv_commit(p, D, in_bf16, ch, cst); });
-        if (e != cudaSuccess) return cuda_fail(e, "conv-state commit kernel");
     }
     for (int i = 0; i < n; ++i) sessions[i].committed += 1;
     return GDN_OK;

@@ -1,5 +1,5 @@
 // Conv-state commit, state copy (checkpoint capture / restore, session zeroing)
-// and the one-token decode step.
+// and the one-token decode step (which commits its own conv state).
 #include "common.cuh"
 
 namespace gdn {
@@ -46,102 +46,118 @@ __global__ void __launch_bounds__(256) copy2_kernel(uint4 *d0, const uint4 *s0, 
     }
 }
 
-// Sum over the 32 lanes of a warp of 16 per-lane values, scattered: afterwards
-// lanes 2c and 2c + 1 both hold the warp's total of value c (16 shuffles in all).
-__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 16, half = 8; o >= 2; o >>= 1, half >>= 1) {
-        const bool up = lane & o;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = up ? v[i] : v[i + half];
-            const float keep = up ? v[i + half] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-
-// One token of one session: CTA (session, 16-column slice of d_v) x v-head, thread i owns row i of the
-// slice of S^T (d_k x 16, in registers).
+// One token of one session for one q/k head and its G v-heads: CTA (session, q/k head), 256 threads.
+// Thread t owns columns 4 (t % (D/4)) .. + 3 of rows t / (D/4) + NRG i of S^T (NRG = 1024 / D row
+// groups), so every warp-wide access of the state reads or writes whole rows in 16-byte vectors.
 //   u = beta (v - alpha S k),  S^T <- alpha S^T + k u^T,  o = S q
-// (the gated delta rule step with alpha = exp(g)); the conv state is committed by conv_commit_kernel.
+// (the gated delta rule step with alpha = exp(g)). Sums over d_k go in a fixed order: each thread over
+// its rows in increasing order, then the row groups in increasing order, so a session's result does not
+// depend on the batch. The CTA is the only reader of its channels' conv state (q and k of its head, v of
+// its v-heads), and each channel's old state is read by the one thread that writes its new state, so
+// the conv state is committed in place without a separate launch.
 template <int D, typename InT>
-__global__ void __launch_bounds__(D) decode_kernel(const LaunchCommon p, int64_t ch) {
-    constexpr int SC = 16, NW = D / 32, NSL = D / SC;
-    __shared__ float red[2][NW], part[NW][SC], vsh[SC], ush[SC];
-    const int si = blockIdx.x / NSL, sl = blockIdx.x % NSL, c0 = sl * SC;
-    const SessRef s = p.s[si];
-    const int h = blockIdx.y, hk = h / p.G, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+__global__ void __launch_bounds__(256) decode_kernel(const LaunchCommon p, int64_t ch) {
+    constexpr int NT = 256, LPR = D / 4, NRG = NT / LPR, RPT = D / NRG, NW = NT / 32;
+    static_assert(2 * D <= NT && RPT * NRG == D, "thread map");
+    __shared__ float qk[2][D], vv[D], uu[D], red[NRG][D], ss[NW];
+    const SessRef s = p.s[blockIdx.x];
+    const int hk = blockIdx.y, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int c0 = 4 * (t % LPR), rg = t / LPR;
     const int64_t nq = (int64_t)p.Hk * D, nv = (int64_t)p.Hv * D;
     const InT *cw = static_cast<const InT *>(p.conv_w);
-    const InT *cs = static_cast<const InT *>(s.conv);
-    auto conv1 = [&](const void *xp, int64_t ld, int64_t col, int64_t chan) {
+    const InT *cs0 = static_cast<const InT *>(s.conv0);
+    InT *cs = static_cast<InT *>(s.conv);
+    // conv of one channel from its raw input x0 and old state, and the channel's new state [old1, old2, x0]
+    auto conv1 = [&](InT x0, int64_t chan) {
         float w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) w[i] = to_f(cw[chan * 4 + i]);
-        const float x0 = to_f(static_cast<const InT *>(xp)[s.row0 * ld + col]);
-        return conv_tap<InT>(w, to_f(cs[chan]), to_f(cs[ch + chan]), to_f(cs[2 * ch + chan]), x0, p.act);
+        const InT o0 = cs0[chan], o1 = cs0[ch + chan], o2 = cs0[2 * ch + chan];
+        const float y = conv_tap<InT>(w, to_f(o0), to_f(o1), to_f(o2), to_f(x0), p.act);
+        cs[chan] = o1;
+        cs[ch + chan] = o2;
+        cs[2 * ch + chan] = x0;
+        return y;
     };
-    // the slice of S^T: row t, columns c0 .. c0 + 15
-    float *Srow = s.S + (int64_t)h * D * D + (int64_t)t * D + c0;
-    float st[SC];
+    auto load_state = [&](float4 (&st)[RPT], int h) {
+        const float *S0 = s.S0 + (int64_t)h * D * D;
 #pragma unroll
-    for (int c = 0; c < SC; c += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(Srow + c);
-        st[c] = v.x; st[c + 1] = v.y; st[c + 2] = v.z; st[c + 3] = v.w;
-    }
-    const float yq = conv1(p.xq, nq, (int64_t)hk * D + t, (int64_t)hk * D + t);
-    const float yk = conv1(p.xk, nq, (int64_t)hk * D + t, nq + (int64_t)hk * D + t);
-    if (t < SC) vsh[t] = conv1(p.xv, nv, (int64_t)h * D + c0 + t, 2 * nq + (int64_t)h * D + c0 + t);
-    float sq = yq * yq, sk = yk * yk;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        sk += __shfl_xor_sync(0xffffffffu, sk, o);
-    }
-    if (lane == 0) { red[0][warp] = sq; red[1][warp] = sk; }
-    __syncthreads();
-    float tq = 0.f, tk = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) { tq += red[0][w]; tk += red[1][w]; }
-    const float qt = yq * (p.q_scale / sqrtf(tq + p.eps));
-    const float kt = yk * (1.f / sqrtf(tk + p.eps));
-    const float alpha = expf(p.g[s.row0 * p.Hv + h]), b = p.beta[s.row0 * p.Hv + h];
+        for (int i = 0; i < RPT; ++i) st[i] = *reinterpret_cast<const float4 *>(S0 + (int64_t)(rg + NRG * i) * D + c0);
+    };
+    float4 st[RPT];
+    load_state(st, hk * p.G);   // in flight during the conv of q and k
 
-    // (S k)_j over the slice's columns: column sums of k_t S[t][j]
-    float v[SC];
+    // q (threads 0..D-1) and k (threads D..2D-1), L2-normalised into qk
+    if (t < 2 * D) {
+        const int c = t % D;
+        const bool isk = t >= D;
+        const InT *x = static_cast<const InT *>(isk ? p.xk : p.xq);
+        const float y = conv1(x[s.row0 * nq + (int64_t)hk * D + c], (isk ? nq : 0) + (int64_t)hk * D + c);
+        float sq = y * y;
 #pragma unroll
-    for (int c = 0; c < SC; ++c) v[c] = kt * st[c];
-    float r = warp_reduce_scatter16(v);
-    if (!(lane & 1)) part[warp][lane >> 1] = r;
-    __syncthreads();
-    if (t < SC) {
-        float kS = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) kS += part[w][t];
-        ush[t] = b * (vsh[t] - alpha * kS);
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if (lane == 0) ss[warp] = sq;
+        qk[isk][c] = y;
     }
     __syncthreads();
-    // S^T <- alpha S^T + k u^T, written back; o_j = (S q)_j
+    if (t < 2 * D) {
+        const int c = t % D, w0 = t < D ? 0 : D / 32;
+        float tot = 0.f;
 #pragma unroll
-    for (int c = 0; c < SC; ++c) {
-        st[c] = fmaf(kt, ush[c], alpha * st[c]);
-        v[c] = st[c] * qt;
+        for (int w = 0; w < D / 32; ++w) tot += ss[w0 + w];
+        qk[t >= D][c] *= (t < D ? p.q_scale : 1.f) / sqrtf(tot + p.eps);
     }
+
+    for (int gi = 0; gi < p.G; ++gi) {
+        const int h = hk * p.G + gi;
+        if (gi > 0) load_state(st, h);
+        if (t < D) vv[t] = conv1(static_cast<const InT *>(p.xv)[s.row0 * nv + (int64_t)h * D + t], 2 * nq + (int64_t)h * D + t);
+        const float alpha = expf(p.g[s.row0 * p.Hv + h]), b = p.beta[s.row0 * p.Hv + h];
+        __syncthreads();   // q, k, v of this head are in shared memory; red and uu are free
+
+        // (S k) over this thread's rows, then over the row groups
+        float4 pk = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < SC; c += 4) *reinterpret_cast<float4 *>(Srow + c) = make_float4(st[c], st[c + 1], st[c + 2], st[c + 3]);
-    r = warp_reduce_scatter16(v);
-    if (!(lane & 1)) part[warp][lane >> 1] = r;   // the (S k) partials were consumed before the barrier above
-    __syncthreads();
-    if (t < SC) {
-        float o = 0.f;
+        for (int i = 0; i < RPT; ++i) {
+            const float kr = qk[1][rg + NRG * i];
+            pk.x = fmaf(kr, st[i].x, pk.x); pk.y = fmaf(kr, st[i].y, pk.y);
+            pk.z = fmaf(kr, st[i].z, pk.z); pk.w = fmaf(kr, st[i].w, pk.w);
+        }
+        *reinterpret_cast<float4 *>(&red[rg][c0]) = pk;
+        __syncthreads();
+        if (t < D) {
+            float kS = 0.f;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) o += part[w][t];
-        const int64_t oi = (s.row0 * p.Hv + h) * D + c0 + t;
-        if (p.out_bf16) static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(o);
-        else static_cast<float *>(p.out)[oi] = o;
+            for (int r = 0; r < NRG; ++r) kS += red[r][t];
+            uu[t] = b * (vv[t] - alpha * kS);
+        }
+        __syncthreads();
+        // S^T <- alpha S^T + k u^T, written back; o = S q over this thread's rows, then the row groups
+        const float4 u = *reinterpret_cast<const float4 *>(&uu[c0]);
+        float *Sh = s.S + (int64_t)h * D * D;
+        float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int r = rg + NRG * i;
+            const float kr = qk[1][r], qr = qk[0][r];
+            float4 v = st[i];
+            v.x = fmaf(kr, u.x, alpha * v.x); v.y = fmaf(kr, u.y, alpha * v.y);
+            v.z = fmaf(kr, u.z, alpha * v.z); v.w = fmaf(kr, u.w, alpha * v.w);
+            *reinterpret_cast<float4 *>(Sh + (int64_t)r * D + c0) = v;
+            po.x = fmaf(qr, v.x, po.x); po.y = fmaf(qr, v.y, po.y);
+            po.z = fmaf(qr, v.z, po.z); po.w = fmaf(qr, v.w, po.w);
+        }
+        *reinterpret_cast<float4 *>(&red[rg][c0]) = po;   // every read of the (S k) partials preceded the barrier above
+        __syncthreads();
+        if (t < D) {
+            float o = 0.f;
+#pragma unroll
+            for (int r = 0; r < NRG; ++r) o += red[r][t];
+            const int64_t oi = (s.row0 * p.Hv + h) * D + t;
+            if (p.out_bf16) static_cast<__nv_bfloat16 *>(p.out)[oi] = __float2bfloat16_rn(o);
+            else static_cast<float *>(p.out)[oi] = o;
+        }
+        __syncthreads();   // red, vv and uu are read before the next head writes them
     }
 }
 
@@ -169,13 +185,13 @@ cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *d
 
 cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st) {
     using namespace gdn;
-    dim3 grid(p.n_sess * (D / 16), p.Hv);
+    dim3 grid(p.n_sess, p.Hk);
     if (D == 64) {
-        if (in_bf16) decode_kernel<64, __nv_bfloat16><<<grid, 64, 0, st>>>(p, ch);
-        else decode_kernel<64, float><<<grid, 64, 0, st>>>(p, ch);
+        if (in_bf16) decode_kernel<64, __nv_bfloat16><<<grid, 256, 0, st>>>(p, ch);
+        else decode_kernel<64, float><<<grid, 256, 0, st>>>(p, ch);
     } else {
-        if (in_bf16) decode_kernel<128, __nv_bfloat16><<<grid, 128, 0, st>>>(p, ch);
-        else decode_kernel<128, float><<<grid, 128, 0, st>>>(p, ch);
+        if (in_bf16) decode_kernel<128, __nv_bfloat16><<<grid, 256, 0, st>>>(p, ch);
+        else decode_kernel<128, float><<<grid, 256, 0, st>>>(p, ch);
     }
     return cudaGetLastError();
 }
