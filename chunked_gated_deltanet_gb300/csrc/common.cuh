@@ -102,6 +102,9 @@ cudaError_t gdn_take_device_error(unsigned int *out, cudaStream_t st);
 // Device address of the error word on the current device (looked up once per device).
 cudaError_t gdn_device_error_word(unsigned int **out);
 
+// Number of SMs of the current device (looked up once per device).
+cudaError_t gdn_sm_count(int *out);
+
 // Sets the message gdn_last_error() returns on this host thread (library-internal).
 void gdn_internal_set_error(const char *msg);
 

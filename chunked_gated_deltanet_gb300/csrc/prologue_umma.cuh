@@ -1,0 +1,710 @@
+// Prologue + WY/UT transform on the 5th-generation tensor core (tcgen05,
+// accumulators in TMEM), bf16 inputs, d_k = d_v = 128, as a task runner that a
+// kernel calls: a task is one (64-token block, q/k head), for each of the
+// head's G v-heads.
+//
+// The quantities are those of the mma.sync prologue (prep_tc.cu):
+//   conv (kernel 4, halo from the conv state at a call's first block), L2 norm
+//   gamma = cumulative log-decay in the block
+//   A_ij = beta_i e^{gamma_i - gamma_j} (K K^T)_ij (j < i),  T = (I + A)^{-1}
+//   W = T diag(beta e^gamma) K_hat,  U = T diag(beta) V
+//   P_ij = e^{gamma_i - gamma_j} (Q K^T)_ij (j <= i)
+//   Qe = diag(e^gamma) Q_hat - P W,  O_intra = P U,  K_tilde = diag(e^{gamma_63 - gamma_j}) K_hat
+// and the record goes out in the fragment order the state kernel reads.
+//
+// The products run as tcgen05 MMAs of M = 128, issued by one thread, each
+// with bf16 hi/lo operand pairs (hi*hi + hi*lo + lo*hi, about 16 significant
+// bits per operand, fp32 accumulation). P W = (P T) Bk and P U = (P T) Bv, so
+// stacking [T; P T] as the A operand gives all four 64 x 128 results of the
+// block in one product whose every accumulator row is used:
+//   [Q_hat; K_hat] K_hat^T               N = 64,  K = 128 -> TMEM columns 0..63 (kept for every v-head)
+//   P T                                  N = 64,  K = 64  -> TMEM columns 64..127 (rows 64..127 unused)
+//   [T; P T] [beta e^gamma K_hat | beta V] N = 256, K = 64 -> TMEM columns 256..511: [W U; P W P U]
+// Operands live in shared memory in the no-swizzle layouts of umma.cuh: the
+// row-ordered operands (q_hat, k_hat, P, T, P T) K-major, the token-by-channel
+// B operands MN-major, so that every producer writes whole 16-byte
+// core-matrix rows. The triangular inverse stays in fp32 on the CUDA cores.
+// The input tiles arrive as 2-D tensor copies (one per tile) plus three
+// single-row halo copies, on an mbarrier; every wait is bounded, and on a
+// timeout the CTA records it in the device error word, waits (bounded) for
+// what it has in flight and returns (the kernel then frees its TMEM).
+#pragma once
+#include "common.cuh"
+#include "mma.cuh"
+#include "umma.cuh"
+
+namespace gdn {
+
+constexpr int kUmmaPrepThreads = 512;
+
+namespace up {   // shared-memory plan, bytes
+constexpr int D = 128;
+constexpr uint32_t AQ_LBO = 144, AQ_SBO = 16 * AQ_LBO;    // [q_hat; k_hat], K-major, K = 128, 16-byte gap between K cores
+constexpr uint32_t AQ_BYTES = 16 * AQ_SBO;                  // 128 rows
+constexpr uint32_t B_LBO = 128, B_SBO = 8 * B_LBO + 16;     // [beta e^gamma k_hat | beta v], MN-major, N = 256, K = 64
+constexpr uint32_t B_BYTES = 32 * B_SBO;
+constexpr uint32_t K64_LBO = 128, K64_SBO = 8 * K64_LBO;    // K = 64 operands: P, [T; P T] (K-major), T (MN-major)
+constexpr uint32_t R64_BYTES = 8 * K64_SBO;                 // 64 rows (or 64 columns) of a K = 64 operand
+constexpr int LT = kBlock + 4;                              // fp32 A and T row pitch (floats)
+constexpr uint32_t OFF_AQH = 0, OFF_AQL = AQ_BYTES;
+constexpr uint32_t OFF_BH = 2 * AQ_BYTES, OFF_BL = OFF_BH + B_BYTES;
+constexpr uint32_t OFF_PH = OFF_BL + B_BYTES, OFF_PL = OFF_PH + R64_BYTES;     // P, K-major
+constexpr uint32_t OFF_TBH = OFF_PL + R64_BYTES, OFF_TBL = OFF_TBH + R64_BYTES; // T, MN-major (B of P T)
+constexpr uint32_t OFF_AF = OFF_TBL + R64_BYTES;             // fp32 A (input of the inverse)
+constexpr uint32_t OFF_TF = OFF_AF + 4 * kBlock * LT;        // fp32 T
+constexpr uint32_t OFF_MT = OFF_TF + 4 * kBlock * LT;        // 2 x 16 x 24 inverse scratch
+constexpr uint32_t OFF_ATH = OFF_AF, OFF_ATL = OFF_ATH + 2 * R64_BYTES;   // [T; P T], K-major, over A and T
+constexpr uint32_t OFF_SMALL = OFF_MT + 4 * 2 * 16 * 24;     // gamma, beta, e^gamma
+constexpr uint32_t W_BYTES = D * 4 * 2;                      // conv weights of one head's channels (bf16 [D][4])
+constexpr uint32_t OFF_W = OFF_SMALL + 4 * 3 * kBlock;       // q, k, v conv weights
+constexpr uint32_t OFF_BAR = OFF_W + 3 * W_BYTES;            // the control words (UmmaCtl) of the standalone kernel
+constexpr uint32_t SMEM = OFF_BAR + 32;                      // the operand plan ends at OFF_BAR
+constexpr uint32_t RAW_ROW = 2 * D, RAW_TILE = (kBlock + 3) * RAW_ROW;
+constexpr uint32_t TILE_BYTES = RAW_TILE + W_BYTES;           // one staged tile: 64 + 3 rows and its weights
+constexpr uint32_t OFF_RAW = OFF_PH;                         // raw input tiles: dead before P, T, A are written
+static_assert(OFF_RAW + 3 * RAW_TILE <= OFF_SMALL, "raw tiles must fit the P, T and inverse regions");
+static_assert(OFF_ATL + 2 * R64_BYTES <= OFF_MT, "[T; P T] must fit over A and T");
+static_assert(OFF_RAW % 128 == 0 && RAW_TILE % 128 == 0, "tensor-copy destinations 128-byte aligned");
+// the P T product reads 128 A rows from P's low half: the 64 rows after it are T's, in bounds
+static_assert(OFF_PL + 2 * R64_BYTES <= SMEM, "rows read past P's low part");
+static_assert(SMEM <= 227 * 1024, "shared memory");
+}  // namespace up
+
+// Control words of the prologue, kept apart from its operand plan.
+struct UmmaCtl {
+    uint64_t bar[2];   // [0] input copies, [1] MMA groups
+    uint32_t tslot;    // TMEM allocation result
+};
+
+// A persistent CTA's tasks: blockIdx.x, + gridDim.x, ... of the launch's nblk x Hk tasks, task tau =
+// (block tau % nblk, q/k head tau / nblk). A task source hands out task indices in the order the CTA runs
+// them (first(), then next() until it returns -1, all CTA-uniform) and is told when a task's record is
+// complete (done()).
+struct StridedTasks {
+    int tau, ntask;
+    __device__ __forceinline__ int first() { return tau < ntask ? tau : -1; }
+    __device__ __forceinline__ int next() { tau += gridDim.x; return tau < ntask ? tau : -1; }
+    __device__ __forceinline__ void done(int, int) {}
+};
+
+// dst[0] = a, dst[1] = b in one 32-byte store (dst 32-byte aligned)
+__device__ __forceinline__ void st_v8(float4 *dst, float4 a, float4 b) {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"l"(dst), "f"(a.x), "f"(a.y), "f"(a.z), "f"(a.w),
+                 "f"(b.x), "f"(b.y), "f"(b.z), "f"(b.w)
+                 : "memory");
+}
+
+// Each thread of a warp holds row r (r % 16 == lane % 16) of a 16-column chunk
+// starting at column c0 (a multiple of 16). The pair of lanes (l, l ^ 8)
+// holds rows r and r ^ 8 and together writes their m16n8k8 A fragments
+// (float4 per fragment lane) of an operand with K columns: each thread the
+// two adjacent fragment lanes L, L + 1 (L even) in one 32-byte store, so that a
+// store instruction fills whole sectors.
+__device__ __forceinline__ void put_afrag16(float *base, int r, int c0, const float (&v)[16], int K, int lane) {
+    const bool upper = lane & 8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float *w = v + 8 * h;
+        const float p0 = __shfl_xor_sync(0xffffffffu, upper ? w[0] : w[2], 8);
+        const float p1 = __shfl_xor_sync(0xffffffffu, upper ? w[1] : w[3], 8);
+        const float p2 = __shfl_xor_sync(0xffffffffu, upper ? w[4] : w[6], 8);
+        const float p3 = __shfl_xor_sync(0xffffffffu, upper ? w[5] : w[7], 8);
+        const float4 f0 = upper ? make_float4(p0, w[2], p2, w[6]) : make_float4(w[0], p0, w[4], p2);
+        const float4 f1 = upper ? make_float4(p1, w[3], p3, w[7]) : make_float4(w[1], p1, w[5], p3);
+        const int L = 4 * (r & 7) + (upper ? 2 : 0), ks = (c0 >> 3) + h;
+        float4 *dst = reinterpret_cast<float4 *>(base) + (((r >> 4) * (K >> 3) + ks) * 32 + L);
+        st_v8(dst, f0, f1);
+    }
+}
+
+// Same pairing, for row i of a 64 x D accumulator stored by 16-column slices
+// of m16n8 C fragments (cfrag_slice_index order).
+__device__ __forceinline__ void put_cfrag16(float *base, int i, int c0, const float (&v)[16], int lane) {
+    const bool upper = lane & 8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float *w = v + 8 * h;
+        const float p0 = __shfl_xor_sync(0xffffffffu, upper ? w[0] : w[4], 8);
+        const float p1 = __shfl_xor_sync(0xffffffffu, upper ? w[1] : w[5], 8);
+        const float p2 = __shfl_xor_sync(0xffffffffu, upper ? w[2] : w[6], 8);
+        const float p3 = __shfl_xor_sync(0xffffffffu, upper ? w[3] : w[7], 8);
+        const float4 f0 = upper ? make_float4(p0, p1, w[4], w[5]) : make_float4(w[0], w[1], p0, p1);
+        const float4 f1 = upper ? make_float4(p2, p3, w[6], w[7]) : make_float4(w[2], w[3], p2, p3);
+        const int L = 4 * (i & 7) + (upper ? 2 : 0);
+        float4 *dst = reinterpret_cast<float4 *>(base) + ((((c0 >> 4) * 4 + (i >> 4)) * 2 + h) * 32 + L);
+        st_v8(dst, f0, f1);
+    }
+}
+
+// c += X Y for a 16 x K block of X (row-major, pitch lx) and a K x 8 block of Y (row-major, pitch ly),
+// m16n8k8 tf32 MMAs with split operands (hi*hi + hi*lo + lo*hi: close to fp32 products); one warp.
+__device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, int lx, const float *Y, int ly, int K,
+                                               int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(X[g * lx + k0 + t], ah[0], al[0]);
+        split_tf32(X[(g + 8) * lx + k0 + t], ah[1], al[1]);
+        split_tf32(X[g * lx + k0 + t + 4], ah[2], al[2]);
+        split_tf32(X[(g + 8) * lx + k0 + t + 4], ah[3], al[3]);
+        split_tf32(Y[(k0 + t) * ly + g], bh[0], bl[0]);
+        split_tf32(Y[(k0 + t + 4) * ly + g], bh[1], bl[1]);
+        mma_tf32(c, al, bh);
+        mma_tf32(c, ah, bl);
+        mma_tf32(c, ah, bh);
+    }
+}
+// the m16n8 C fragment c (times s) into a row-major block Z (pitch lz)
+__device__ __forceinline__ void store_c16x8(float *Z, int lz, const float (&c)[4], float s, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2 *>(Z + g * lz + 2 * t) = make_float2(s * c[0], s * c[1]);
+    *reinterpret_cast<float2 *>(Z + (g + 8) * lz + 2 * t) = make_float2(s * c[2], s * c[3]);
+}
+
+// 8 fp32 values -> bf16 hi and lo halves, packed for one 16-byte core-matrix row each
+__device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        __nv_bfloat16 h0, l0, h1, l1;
+        split_bf16(v[2 * q], h0, l0);
+        split_bf16(v[2 * q + 1], h1, l1);
+        h[q] = pack_bf16(h0, h1);
+        l[q] = pack_bf16(l0, l1);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// hi + lo of 8 bf16 pairs (one core-matrix row of each half)
+__device__ __forceinline__ void join8(uint4 hi, uint4 lo, float *v) {
+    const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w}, l[4] = {lo.x, lo.y, lo.z, lo.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = __uint_as_float(h[q] << 16) + __uint_as_float(l[q] << 16);
+        v[2 * q + 1] = __uint_as_float(h[q] & 0xFFFF0000u) + __uint_as_float(l[q] & 0xFFFF0000u);
+    }
+}
+
+// Runs the tasks that `src` hands out, in order, on the operand plan at `sm` with control words `ctl` and
+// 512 TMEM columns at `tmem` (allocated by the caller); every thread of the CTA (512) calls it. A task is
+// one (64-token block, q/k head) with each of the head's G v-heads; the next task's inputs are staged
+// during the current task's record epilogue. Returns false if a bounded wait ran out (the error word is
+// set, nothing is left in flight). The mbarriers are initialised on entry and invalidated on return, so
+// the plan's memory may serve other uses between calls.
+template <class Src>
+__device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, unsigned char *sm, UmmaCtl *ctl,
+                                             uint32_t tmem, Src &src) {
+    using namespace up;
+    unsigned char *AQh = sm + OFF_AQH, *AQl = sm + OFF_AQL, *Bh = sm + OFF_BH, *Bl = sm + OFF_BL;
+    unsigned char *Ph = sm + OFF_PH, *Pl = sm + OFF_PL, *TBh = sm + OFF_TBH, *TBl = sm + OFF_TBL;
+    unsigned char *ATh = sm + OFF_ATH, *ATl = sm + OFF_ATL;
+    float *Af = reinterpret_cast<float *>(sm + OFF_AF), *Tf = reinterpret_cast<float *>(sm + OFF_TF);
+    float *Mt = reinterpret_cast<float *>(sm + OFF_MT);
+    float *gam = reinterpret_cast<float *>(sm + OFF_SMALL), *bet = gam + kBlock, *egv = bet + kBlock;
+    uint64_t *bar = ctl->bar;
+    __nv_bfloat16 *rawq = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_RAW);
+    __nv_bfloat16 *rawk = rawq + (kBlock + 3) * D, *rawv = rawk + (kBlock + 3) * D;
+    __nv_bfloat16 *wq = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W), *wk = wq + 4 * D, *wv = wk + 4 * D;
+
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int Hk = p.Hk, Hv = p.Hv;
+    const int64_t nq = (int64_t)Hk * D, nv = (int64_t)Hv * D;
+    const __nv_bfloat16 *cw = static_cast<const __nv_bfloat16 *>(p.conv_w);
+    struct Task { int blk, hk, pos0, n; int64_t row0; SessRef s; };
+    auto task_of = [&](int tau) {
+        Task k;
+        k.blk = tau % p.nblk;
+        k.hk = tau / p.nblk;
+        k.s = p.s[find_session(p, k.blk)];
+        k.pos0 = (k.blk - k.s.blk0) * kBlock;
+        k.n = min(kBlock, k.s.n - k.pos0);
+        k.row0 = k.s.row0 + k.pos0;
+        return k;
+    };
+    if (t == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    int tau = src.first();
+    if (tau < 0) {
+        if (t == 0) { mbar_inval(&bar[0]); mbar_inval(&bar[1]); }
+        __syncthreads();
+        return true;
+    }
+    Task cur = task_of(tau), nxt = cur;
+    int blk = cur.blk, hk = cur.hk, n = cur.n, ntau = -1;
+    uint32_t in_phase = 0, mma_phase = 0;
+    int in_pending = 0, mma_pending = 0;   // an issued copy group / MMA group not yet seen complete (CTA-uniform)
+
+    // Stage rows pos0-3 .. pos0+63 of task k's q and k tiles (with_qk) and of v-head h's v tile, with their
+    // conv weights: one tensor copy of the block's 64 rows per tile (rows past the inputs read as zero, rows
+    // past n belong to other tokens and only reach masked results), issued by thread 0 with the byte count;
+    // the three halo rows (from the inputs or, before a call's first token, from the conv state) and the
+    // weights as single bulk copies, one per warp 1.., so that no warp waits on them.
+    struct Tile { __nv_bfloat16 *dst, *wdst; const CUtensorMap *map; const __nv_bfloat16 *x; int64_t ld, col0, chan0; };
+    auto tile_of = [&](int q, const Task &k, int h) -> Tile {
+        if (q == 0) return {rawq, wq, &p.tm_q, static_cast<const __nv_bfloat16 *>(p.xq), nq, (int64_t)k.hk * D, (int64_t)k.hk * D};
+        if (q == 1)
+            return {rawk, wk, &p.tm_k, static_cast<const __nv_bfloat16 *>(p.xk), nq, (int64_t)k.hk * D, nq + (int64_t)k.hk * D};
+        return {rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)h * D, 2 * nq + (int64_t)h * D};
+    };
+    auto stage = [&](const Task &k, int h, bool with_qk, bool skip) {
+        in_pending = 1;
+        if (skip) return;
+        const int q0 = with_qk ? 0 : 2, ntile = 3 - q0;
+        // the region was last written by generic stores (ordered by the barriers since): order them
+        // before the async-proxy writes of the copies
+        if (t == 0 || (lane == 0 && warp >= 1 && warp <= 4 * ntile)) fence_proxy_async();
+        if (t == 0) {
+            mbar_arrive_expect_tx(&bar[0], (uint32_t)ntile * TILE_BYTES);
+            for (int q = q0; q < 3; ++q) {
+                const Tile tl = tile_of(q, k, h);
+                tma_load_2d(tl.dst + 3 * D, tl.map, (int)tl.col0, (int)k.row0, &bar[0]);
+            }
+        }
+        if (lane == 0 && warp >= 1 && warp <= 4 * ntile) {
+            const int e = warp - 1, r = e & 3;
+            const Tile tl = tile_of(q0 + (e >> 2), k, h);
+            if (r < 3) {
+                const int pos = k.pos0 - 3 + r;
+                const __nv_bfloat16 *src = pos < 0 ? static_cast<const __nv_bfloat16 *>(k.s.conv0) + (int64_t)(3 + pos) * ch + tl.chan0
+                                                   : tl.x + (k.s.row0 + pos) * tl.ld + tl.col0;
+                bulk_g2s(tl.dst + r * D, src, RAW_ROW, &bar[0]);
+            } else {
+                bulk_g2s(tl.wdst, cw + tl.chan0 * 4, W_BYTES, &bar[0]);
+            }
+        }
+    };
+    // every thread waits; true when the phase completed for all of them (CTA-uniform)
+    auto wait_in = [&]() {
+        const bool ok = mbar_wait_bounded(&bar[0], in_phase, p.wait_limit);
+        if (__syncthreads_or(!ok)) return false;
+        in_phase ^= 1u;
+        in_pending = 0;
+        return true;
+    };
+    auto wait_mma = [&]() {
+        const bool ok = mbar_wait_bounded(&bar[1], mma_phase, p.wait_limit);
+        if (__syncthreads_or(!ok)) return false;
+        mma_phase ^= 1u;
+        mma_pending = 0;
+        tc_fence_after();
+        return true;
+    };
+    // bf16 hi/lo MMA group D (+)= A B over K (3 passes per 16-wide K-step), then a commit; thread 0 only
+    auto mma3 = [&](uint32_t d, uint64_t ah, uint64_t al, uint32_t astep, uint64_t bh, uint64_t bl, uint32_t bstep,
+                    int K, uint32_t id) {
+        tc_fence_after();
+        for (int ks = 0; ks < K / 16; ++ks) {
+            const uint64_t oa = (astep * ks) >> 4, ob = (bstep * ks) >> 4;
+            umma_bf16(d, ah + oa, bh + ob, id, ks > 0);
+            umma_bf16(d, ah + oa, bl + ob, id, 1);
+            umma_bf16(d, al + oa, bh + ob, id, 1);
+        }
+        umma_commit(&bar[1]);
+    };
+
+    // Row-parallel conv of rows [r0, r0 + nr) of a staged tile: lane owns channels 4 lane .. 4 lane + 3,
+    // four rows at a time; outputs go through emit(i0, y[4][4]).
+    auto conv_rows = [&](const __nv_bfloat16 *raw, const __nv_bfloat16 *wsm, int r0, int nr, auto &&emit) {
+        float w[4][4];
+        {
+            const uint4 u0 = *reinterpret_cast<const uint4 *>(wsm + lane * 16);
+            const uint4 u1 = *reinterpret_cast<const uint4 *>(wsm + lane * 16 + 8);
+            const uint32_t ww[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                w[e >> 1][2 * (e & 1)] = __uint_as_float(ww[e] << 16);
+                w[e >> 1][2 * (e & 1) + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+            }
+        }
+        for (int i0 = r0; i0 < r0 + nr; i0 += 4) {
+            float x[7][4];   // raw rows i0 .. i0+6 = block rows i0-3 .. i0+3
+#pragma unroll
+            for (int r = 0; r < 7; ++r) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(raw + (i0 + r) * D + lane * 4);
+                const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+                x[r][0] = __low2float(a); x[r][1] = __high2float(a); x[r][2] = __low2float(b); x[r][3] = __high2float(b);
+            }
+            float y[4][4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    y[u][c] = conv_tap<__nv_bfloat16>(w[c], x[u][c], x[u + 1][c], x[u + 2][c], x[u + 3][c], 0);
+            if (p.act) {   // SiLU, as one branch after the taps so that the default path stays compact
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) y[u][c] = y[u][c] / (1.0f + expf(-y[u][c]));
+            }
+            emit(i0, y);
+        }
+    };
+    auto split4_store = [&](unsigned char *hi, unsigned char *lo, uint32_t off, const float (&v)[4]) {
+        __nv_bfloat16 h[4], l[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) split_bf16(v[c], h[c], l[c]);
+        *reinterpret_cast<uint2 *>(hi + off) = make_uint2(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]));
+        *reinterpret_cast<uint2 *>(lo + off) = make_uint2(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]));
+    };
+    auto store8 = [&](unsigned char *hi, unsigned char *lo, uint32_t off, const float *v) {
+        uint4 h, l;
+        split8(v, h, l);
+        *reinterpret_cast<uint4 *>(hi + off) = h;
+        *reinterpret_cast<uint4 *>(lo + off) = l;
+    };
+
+    // beta v of the staged v-head (row-parallel conv, 4 rows per warp) into channels 128..255 of the B operand
+    auto conv_v = [&]() {
+        conv_rows(rawv, wv, 4 * warp, 4, [&](int i0, float (&y)[4][4]) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                float v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = i < n ? bet[i] * y[u][c] : 0.f;
+                split4_store(Bh, Bl, mnmajor_bf16_offset(128 + 4 * lane, i, B_LBO, B_SBO), v);
+            }
+        });
+    };
+
+    stage(cur, hk * p.G, true, p.debug_skip_first_copy == 2);   // 1. the first task's tiles
+    // gamma (inclusive scan of g over the block), beta and e^gamma of v-head h, by warps 2 and 3 alone: warp 3
+    // adds the total of rows 0..31 itself, so no barrier is needed. The loads can be issued early (for the
+    // next task, during the current one's record epilogue) and the scan run later.
+    const int jg = t - 64;
+    struct Gv { float g, b, lo; };
+    auto gates_load = [&](const Task &k, int h) {
+        Gv r{0.f, 0.f, 0.f};
+        if (jg < 0 || jg >= kBlock) return r;
+        if (jg < k.n) {
+            r.g = p.g[(k.row0 + jg) * Hv + h];
+            r.b = p.beta[(k.row0 + jg) * Hv + h];
+        }
+        if (jg >= 32 && lane < k.n) r.lo = p.g[(k.row0 + lane) * Hv + h];
+        return r;
+    };
+    auto gates_store = [&](Gv r) {
+        if (jg < 0 || jg >= kBlock) return;
+        float sv = r.g, lo = r.lo;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, sv, o);
+            if (lane >= o) sv += y;
+        }
+        if (jg >= 32) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lo += __shfl_xor_sync(0xffffffffu, lo, o);
+            sv += lo;
+        }
+        gam[jg] = sv;
+        bet[jg] = r.b;
+        egv[jg] = expf(sv);
+    };
+    gates_store(gates_load(cur, hk * p.G));
+    Gv gnext{0.f, 0.f, 0.f};
+    bool ok = true;
+    for (;;) {   // tasks
+    ok = wait_in();
+
+    if (ok) {
+        // 2. conv + L2 norm of q (warps 0-7) and k (warps 8-15), 8 rows per warp -> bf16 hi/lo rows of [q_hat; k_hat]
+        const int which = warp >> 3;
+        const float qs = which ? 1.f : p.q_scale;
+        conv_rows(which ? rawk : rawq, which ? wk : wq, 8 * (warp & 7), 8, [&](int i0, float (&y)[4][4]) {
+            float ss[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                ss[u] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ss[u] = fmaf(y[u][c], y[u][c], ss[u]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u;
+                const float scale = qs * rsqrtf(ss[u] + p.eps);
+                float v[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) v[c] = i < n ? y[u][c] * scale : 0.f;
+                split4_store(AQh, AQl, kmajor_bf16_offset(64 * which + i, 4 * lane, AQ_LBO, AQ_SBO), v);
+            }
+        });
+        conv_v();   // the first v-head's beta v in the same phase
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        // 3. [Q K^T; K K^T] = [q_hat; k_hat] k_hat^T into TMEM columns 0..63
+        if (t == 0)
+            mma3(tmem, umma_smem_desc(AQh, AQ_LBO, AQ_SBO), umma_smem_desc(AQl, AQ_LBO, AQ_SBO), 2 * AQ_LBO,
+                 umma_smem_desc(AQh + 8 * AQ_SBO, AQ_LBO, AQ_SBO), umma_smem_desc(AQl + 8 * AQ_SBO, AQ_LBO, AQ_SBO),
+                 2 * AQ_LBO, D, umma_idesc_bf16(128, 64, 0, 0));
+        mma_pending = 1;
+    }
+
+    // 4. each v-head of the group
+    for (int gi = 0; ok && gi < p.G; ++gi) {
+        const int h = hk * p.G + gi;
+        if (gi > 0) {   // the previous head is done with the raw-tile region and every MMA operand
+            stage(cur, h, false, false);
+            gates_store(gates_load(cur, h));
+            if (!(ok = wait_in())) break;
+        }
+        float *rec = p.ws_wu + ((int64_t)blk * Hv + h) * rec_floats(D);
+        // K_tilde^T as tf32 A fragments (D x 64), half `part` of its float4 groups, by warps 1-15 (warp 0
+        // issues the MMAs); e^{gamma_63} with the first half
+        auto kt_record = [&](int part) {
+            if (warp == 0) return;
+            constexpr int NG = (D / 16) * 8 * 32, HALF = NG / 2;
+            const float gl = gam[kBlock - 1];
+            for (int e = HALF * part + t - 32; e < HALF * (part + 1); e += kUmmaPrepThreads - 32) {
+                const int ln = e & 31, tile = e >> 5, mt = tile >> 3, ks = tile & 7, gg = ln >> 2, tt = ln & 3;
+                float v[4];
+#pragma unroll
+                for (int f = 0; f < 4; ++f) {
+                    const int m = 16 * mt + gg + 8 * (f & 1), k = 8 * ks + tt + 4 * (f >> 1);
+                    const uint32_t o = kmajor_bf16_offset(kBlock + k, m, AQ_LBO, AQ_SBO);
+                    const float kh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQh + o)) +
+                                     __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQl + o));
+                    v[f] = tf32_round(__expf(gl - gam[k]) * kh);
+                }
+                *reinterpret_cast<float4 *>(rec + 128 * D + e * 4) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+            if (part == 0 && t == 32) rec[320 * D] = expf(gl);
+        };
+
+        // 5. B operand, MN-major: channels 128..255 = beta v (the first v-head's came with the q/k conv),
+        //    channels 0..127 = beta e^gamma k_hat (from the hi/lo rows)
+        if (gi > 0) conv_v();
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int j = t & 63, cg = (t >> 6) + 8 * it;
+            const uint32_t o = kmajor_bf16_offset(64 + j, 8 * cg, AQ_LBO, AQ_SBO);
+            float v[8];
+            join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), v);
+            const float sc = bet[j] * egv[j];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v[c] *= sc;
+            store8(Bh, Bl, mnmajor_bf16_offset(8 * cg, j, B_LBO, B_SBO), v);
+        }
+        fence_proxy_async();
+        if (gi == 0) {
+            if (!(ok = wait_mma())) break;   // Q K^T / K K^T landed in TMEM
+        } else {
+            __syncthreads();
+        }
+
+        // 6. from TMEM: P (rows 0..63 -> bf16 hi/lo K-major) and A (rows 64..127 -> fp32)
+        {
+            const int q = warp & 3, cp = warp >> 2, R = 32 * q + lane, j0 = 16 * cp;
+            uint32_t r[16];
+            tmem_ld16_nowait(tmem + ((uint32_t)(32 * q) << 16) + j0, r);
+            float dec[16];   // e^{gamma_i - gamma_j}, while the load is in flight
+            {
+                const float gr = gam[R < kBlock ? R : R - kBlock];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) dec[jj] = __expf(gr - gam[j0 + jj]);
+            }
+            tmem_wait_ld(r);
+            float v[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) v[jj] = __uint_as_float(r[jj]);
+            if (R < kBlock) {
+                const int i = R;
+                float pv[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) pv[jj] = (j0 + jj) <= i ? v[jj] * dec[jj] : 0.f;
+                store8(Ph, Pl, kmajor_bf16_offset(i, j0, K64_LBO, K64_SBO), pv);
+                store8(Ph, Pl, kmajor_bf16_offset(i, j0 + 8, K64_LBO, K64_SBO), pv + 8);
+            } else {
+                const int i = R - kBlock;
+                float av[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) av[jj] = (j0 + jj) < i ? bet[i] * dec[jj] * v[jj] : 0.f;
+#pragma unroll
+                for (int c = 0; c < 16; c += 4)
+                    *reinterpret_cast<float4 *>(Af + i * LT + j0 + c) = make_float4(av[c], av[c + 1], av[c + 2], av[c + 3]);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // 7. T = (I + A)^{-1} (unit lower triangular) in fp32, two levels of 2x2 blocking:
+        //    diagonal 16x16 blocks D_b by substitution (one column per thread; the other threads zero the
+        //    blocks above the diagonal), then T_10 = -D_1 A_10 D_0 and T_32 = -D_3 A_32 D_2, then
+        //    T[32:64, 0:32] = -T[32:64, 32:64] A[32:64, 0:32] T[0:32, 0:32]; products as split-tf32 MMAs
+        if (t < kBlock) {
+            const int d = t >> 4, c = t & 15;
+            const float *Ad = Af + 16 * d * LT + 16 * d;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float sum = 0.f;
+#pragma unroll
+                for (int j = 0; j < i; ++j)
+                    if (j >= c) sum = fmaf(Ad[i * LT + j], x[j], sum);
+                x[i] = i < c ? 0.f : (i == c ? 1.f : -sum);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tf[(16 * d + i) * LT + 16 * d + c] = x[i];
+        } else {
+            for (int e = t - kBlock; e < 6 * 64; e += kUmmaPrepThreads - kBlock) {   // 6 blocks x 16 rows x 4 float4
+                const int bi = e >> 6, r = (e >> 2) & 15, c4 = e & 3;
+                const int ib = bi < 3 ? 0 : (bi < 5 ? 1 : 2), jb = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
+                *reinterpret_cast<float4 *>(Tf + (16 * ib + r) * LT + 16 * jb + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        __syncthreads();
+        constexpr int LM = 24, LX = 40;
+        float *Xs = reinterpret_cast<float *>(TBh);   // 32 x LX scratch (the T operand regions are written later)
+        if (warp < 4) {   // warps 0,1: block pair (1, 0); warps 2,3: (3, 2); 8 columns each
+            const int b = 2 * (warp >> 1), nt = warp & 1;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3_tf32_16x8(c, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, 16, lane);
+            store_c16x8(Mt + (warp >> 1) * 16 * LM + 8 * nt, LM, c, 1.f, lane);
+        }
+        __syncthreads();
+        if (warp < 4) {
+            const int b = 2 * (warp >> 1), nt = warp & 1;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3_tf32_16x8(c, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, Mt + (warp >> 1) * 16 * LM + 8 * nt, LM, 16, lane);
+            store_c16x8(Tf + 16 * (b + 1) * LT + 16 * b + 8 * nt, LT, c, -1.f, lane);
+        }
+        __syncthreads();
+        if (warp < 8) {   // X = A[32:64, 0:32] T[0:32, 0:32]: 2 m-tiles x 4 n-tiles
+            const int mt = warp >> 2, nt = warp & 3;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3_tf32_16x8(c, Af + (32 + 16 * mt) * LT, LT, Tf + 8 * nt, LT, 32, lane);
+            store_c16x8(Xs + 16 * mt * LX + 8 * nt, LX, c, 1.f, lane);
+        }
+        __syncthreads();
+        if (warp < 8) {   // T[32:64, 0:32] = -T[32:64, 32:64] X
+            const int mt = warp >> 2, nt = warp & 3;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            mma3_tf32_16x8(c, Tf + (32 + 16 * mt) * LT + 32, LT, Xs + 8 * nt, LX, 32, lane);
+            store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, c, -1.f, lane);
+        }
+        __syncthreads();
+        //    T as bf16 hi/lo: rows 0..63 of [T; P T] (K-major, written over A and T) and the B operand of
+        //    P T (MN-major)
+        {
+            const int i = t & 63, kg = t >> 6;
+            float v[8];
+            const float4 a = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg);
+            const float4 b = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg + 4);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            __syncthreads();   // every row of T is read before the first write over it
+            store8(ATh, ATl, kmajor_bf16_offset(i, 8 * kg, K64_LBO, K64_SBO), v);
+            store8(TBh, TBl, mnmajor_bf16_offset(8 * kg, i, K64_LBO, K64_SBO), v);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+
+        // 8. P T into TMEM columns 64..127; meanwhile the first half of the K_tilde^T record
+        if (t == 0)
+            mma3(tmem + 64, umma_smem_desc(Ph, K64_LBO, K64_SBO), umma_smem_desc(Pl, K64_LBO, K64_SBO), 2 * K64_LBO,
+                 umma_smem_desc(TBh, K64_LBO, K64_SBO), umma_smem_desc(TBl, K64_LBO, K64_SBO), 2 * K64_LBO, kBlock,
+                 umma_idesc_bf16(128, 64, 0, 1));
+        mma_pending = 1;
+        kt_record(0);   // the first half of K_tilde^T while the product runs, the second under the next one
+        if (!(ok = wait_mma())) break;
+
+        // 9. P T (lanes 0..63; warps 0,1,4,5,8,9,12,13, 16 columns each) -> rows 64..127 of [T; P T]
+        if ((warp & 3) < 2) {
+            const int i = 32 * (warp & 3) + lane, c0 = 16 * (warp >> 2);
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 + c0, v);
+            store8(ATh, ATl, kmajor_bf16_offset(kBlock + i, c0, K64_LBO, K64_SBO), v);
+            store8(ATh, ATl, kmajor_bf16_offset(kBlock + i, c0 + 8, K64_LBO, K64_SBO), v + 8);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+
+        // 10. [W U; P W P U] = [T; P T] [beta e^gamma k_hat | beta v] into TMEM columns 256..511
+        if (t == 0)
+            mma3(tmem + 256, umma_smem_desc(ATh, K64_LBO, K64_SBO), umma_smem_desc(ATl, K64_LBO, K64_SBO), 2 * K64_LBO,
+                 umma_smem_desc(Bh, B_LBO, B_SBO), umma_smem_desc(Bl, B_LBO, B_SBO), 2 * B_LBO, kBlock,
+                 umma_idesc_bf16(128, 256, 0, 1));
+        mma_pending = 1;
+        kt_record(1);
+        if (!(ok = wait_mma())) break;
+
+        // the next task's inputs: the raw-tile region and the weights are free from here on
+        if (gi == p.G - 1 && (ntau = src.next()) >= 0) {
+            nxt = task_of(ntau);
+            stage(nxt, nxt.hk * p.G, true, false);
+            gnext = gates_load(nxt, nxt.hk * p.G);
+        }
+        // 11. the record, every warp (lanes 32 (warp % 4) .., 64 columns at 64 (warp / 4)):
+        //     W rows -> tf32 A fragments (rows 0..63 of [W; Qe]); U rows -> C fragments;
+        //     P W rows -> Qe = e^gamma q_hat - P W (rows 64..127 of [W; Qe]); P U rows -> O_intra C fragments
+        {
+            const int R = 32 * (warp & 3) + lane, cp = warp >> 2;
+            const bool top = R < kBlock;
+            const int i = top ? R : R - kBlock;
+            const uint32_t tb = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 + 64 * cp;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c0 = 64 * cp + 16 * cc;
+                float v[16];
+                tmem_ld16(tb + 16 * cc, v);
+                if (c0 < D) {
+                    if (top) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) v[c] = tf32_round(v[c]);
+                    } else {
+                        float qh[16];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const uint32_t o = kmajor_bf16_offset(i, c0 + 8 * hh, AQ_LBO, AQ_SBO);
+                            join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), qh + 8 * hh);
+                        }
+                        const float e = egv[i];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) v[c] = tf32_round(e * qh[c] - v[c]);
+                    }
+                    put_afrag16(rec, R, c0, v, D, lane);
+                } else {
+                    put_cfrag16(rec + (top ? 192 : 256) * D, i, c0 - D, v, lane);
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();   // TMEM columns and every operand region are free for the next v-head
+    }
+    if (!ok) break;
+    src.done(blk, hk);   // the task's record is complete
+    if (ntau < 0) break;
+    tau = ntau;
+    cur = nxt;
+    blk = cur.blk; hk = cur.hk; n = cur.n;
+    gates_store(gnext);
+    }   // tasks
+
+    if (!ok) {   // a bounded wait ran out: record it and wait (bounded) for what is still in flight
+        if (t == 0) {
+            atomicOr(p.err, 1u);
+            if (in_pending && p.debug_skip_first_copy != 2) mbar_wait_bounded(&bar[0], in_phase, p.wait_limit);
+            if (mma_pending) mbar_wait_bounded(&bar[1], mma_phase, p.wait_limit);
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    tc_fence_after();
+    if (t == 0) { mbar_inval(&bar[0]); mbar_inval(&bar[1]); }
+    __syncthreads();
+    return ok;
+}
+
+
+}  // namespace gdn
