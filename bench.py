@@ -270,67 +270,104 @@ class ReplayStep:
                              flags=g.GDN_ALLOW_PARTIAL)
         g.gdn_state_restore(d, s, slot)
 
+    # call groups of the end-to-end copies (calls per copy; chosen by a sweep on the GB300 machine: 4 calls per
+    # upload and 2 per download gave the shortest step, about 10 % below one copy per call and tensor)
+    up_group = 4
+    down_group = 2
+
+    def up_sizes(self, n):
+        return [self.up_group] * (-(-n // self.up_group))
+
+    def down_sizes(self, n):
+        return [self.down_group] * (-(-n // self.down_group))
+
     def _e2e_setup(self):
-        """Copy plan of the end-to-end step: per turn, the new input rows (host -> device) and the output rows
-        it produces (device -> host), as raw pointers; two copy streams and the events that order them."""
+        """Copy plan of the end-to-end step. Every copy costs a few microseconds of idle host link, so inputs
+        go up in fewer, larger copies: the gates and conv weights of the whole step first, then the q/k/v rows
+        of groups of calls (a call waits only for its group); outputs come down by groups of calls. Groups
+        that are too large make the compute wait for the link. Raw pointers, two copy streams and the events
+        that order them."""
         torch = self.torch
         self.rt = CudaRuntime()
         self.h2d, self.d2h = torch.cuda.Stream(), torch.cuda.Stream()
         row_bytes = [(t.stride(0) * t.element_size(), d.data_ptr(), t.data_ptr()) for d, t in zip(self.x, self.host)]
         out_row = self.out.stride(0) * self.out.element_size()
+        spans = [(a, b, take) for a, b, take in self.calls] + [(self.fork[0], self.fork[1], self.fork[1] - self.fork[0])]
+        n = len(spans)
 
-        def ups(a, b):
-            return [(dp + a * rb, hp + a * rb, (b - a) * rb) for rb, dp, hp in row_bytes]
+        def groups(sizes):
+            out, k = [], 0
+            for g in sizes:
+                if k >= n:
+                    break
+                out.append((k, min(n, k + g)))
+                k += g
+            if k < n:
+                out.append((k, n))
+            return out
 
-        def down(a, b):
-            return (self.host_out.data_ptr() + a * out_row, self.out.data_ptr() + a * out_row, (b - a) * out_row)
-
-        self.plan, prev = [], 0
-        for a, end, take in self.calls:
-            self.plan.append((ups(prev, end), down(a, a + take)))
-            prev = end
-        self.plan_fork = (ups(prev, self.rows), down(*self.fork))
-        self.ev = [self.rt.event() for _ in range(2 * len(self.calls) + 4)]
+        # uploads: whole-step gates and weights, then q, k, v rows by call group
+        self.up_first = [(rb_dp_hp[1], rb_dp_hp[2], self.rows * rb_dp_hp[0]) for rb_dp_hp in row_bytes[3:]]
+        self.up_first.append((self.cw.data_ptr(), self.host_cw.data_ptr(), self.cw.numel() * self.cw.element_size()))
+        self.up_groups, self.up_of = [], [0] * n
+        for gi, (k0, k1) in enumerate(groups(self.up_sizes(n))):
+            r0 = spans[k0 - 1][1] if k0 > 0 else 0
+            r1 = spans[k1 - 1][1]
+            self.up_groups.append([(dp + r0 * rb, hp + r0 * rb, (r1 - r0) * rb) for rb, dp, hp in row_bytes[:3]])
+            for k in range(k0, k1):
+                self.up_of[k] = gi
+        # downloads: committed output rows by call group, issued after the group's last call
+        self.down_after = {}
+        for k0, k1 in groups(self.down_sizes(n)):
+            r0, r1 = spans[k0][0], spans[k1 - 1][0] + spans[k1 - 1][2]
+            self.down_after[k1 - 1] = (self.host_out.data_ptr() + r0 * out_row, self.out.data_ptr() + r0 * out_row,
+                                       (r1 - r0) * out_row)
+        self.n_copies = len(self.up_first) + 3 * len(self.up_groups) + len(self.down_after)
+        self.ev = [self.rt.event() for _ in range(len(self.up_groups) + n + 4)]
 
     def e2e_step(self):
-        """The step through host buffers: each turn's new input rows go up on a copy stream ahead of the
-        compute, and each turn's output rows come back on another copy stream as soon as the turn is done.
+        """The step through host buffers: inputs go up on a copy stream ahead of the compute (each call waits
+        for the upload group that holds its rows), outputs come back on another copy stream by call group.
         The compute stream waits for the last download, so every copy is inside the caller's timed region."""
         g, torch = self.gdn, self.torch
-        if not hasattr(self, "plan"):
+        if not hasattr(self, "up_groups"):
             self._e2e_setup()
         rt, ev = self.rt, self.ev
         comp = torch.cuda.current_stream().cuda_stream
         h2d, d2h = self.h2d.cuda_stream, self.d2h.cuda_stream
         rt.record(ev[-1], comp)
         rt.wait(h2d, ev[-1])                 # the previous step no longer reads the device inputs
-        rt.h2d(self.cw.data_ptr(), self.host_cw.data_ptr(), self.cw.numel() * self.cw.element_size(), h2d)
-        n_calls = len(self.calls)
-        for k, (up, _) in enumerate(self.plan + [self.plan_fork]):
-            for dst, src, nb in up:
+        for dst, src, nb in self.up_first:
+            rt.h2d(dst, src, nb, h2d)
+        for gi, grp in enumerate(self.up_groups):
+            for dst, src, nb in grp:
                 rt.h2d(dst, src, nb, h2d)
-            rt.record(ev[k], h2d)
+            rt.record(ev[gi], h2d)
         d, s, x, cw, out, ws = self.desc, self.sess, self.x, self.cw, self.out, self.ws
+        nG = len(self.up_groups)
 
-        def download(k, spec):
-            rt.record(ev[n_calls + 1 + k], comp)
-            rt.wait(d2h, ev[n_calls + 1 + k])
-            rt.d2h(*spec, d2h)
+        def after(k):
+            spec = self.down_after.get(k)
+            if spec is not None:
+                rt.record(ev[nG + k], comp)
+                rt.wait(d2h, ev[nG + k])
+                rt.d2h(*spec, d2h)
 
         g.gdn_session_init(d, s)
         for k, (a, b, take) in enumerate(self.calls):
-            rt.wait(comp, ev[k])
+            rt.wait(comp, ev[self.up_of[k]])
             slot = self.slots[k % len(self.slots)]
             n = g.gdn_prefill_chunks_checkpoint(d, s, slot, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b],
                                                 cw, out[a:b], ws)
             assert n == take
-            download(k, self.plan[k][1])
+            after(k)
         a, b = self.fork
-        rt.wait(comp, ev[n_calls])
+        k = len(self.calls)
+        rt.wait(comp, ev[self.up_of[k]])
         g.gdn_prefill_chunks(d, s, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b], cw, out[a:b], ws,
                              flags=g.GDN_ALLOW_PARTIAL)
         g.gdn_state_restore(d, s, slot)
-        download(n_calls, self.plan_fork[1])
+        after(k)
         rt.record(ev[-2], d2h)
         rt.wait(comp, ev[-2])
 
@@ -507,6 +544,47 @@ def decode_measure(w, dev, n_sess: int = 64, steps: int = 50):
             "achieved_gbs": round(gbs, 1), "peak_gbs": peak, "frac": round(gbs / peak, 4), "bound": "hbm"}
 
 
+def host_link_measure(step, reps: int = 3):
+    """Host link speed on this machine, with the step's own pinned buffers: every input tensor up, the output
+    down, and both at once (one large copy per tensor, copy streams timed by events); the step's copy floor
+    is its bytes over those speeds."""
+    import torch
+    ups = [(d, h) for d, h in zip(step.x, step.host)]
+    down = (step.host_out, step.out)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    def up():
+        with torch.cuda.stream(s1):
+            for d, h in ups:
+                d.copy_(h, non_blocking=True)
+
+    def dn():
+        with torch.cuda.stream(s2):
+            down[0].copy_(down[1], non_blocking=True)
+
+    def both():
+        up()
+        dn()
+
+    hb = sum(h.numel() * h.element_size() for _, h in ups)
+    db = down[1].numel() * down[1].element_size()
+    t_up, t_dn, t_both = timed(up), timed(dn), timed(both)
+    floor_ms = max(t_up * step.h2d_bytes / hb, t_dn * step.d2h_bytes / db,
+                   t_both * (step.h2d_bytes + step.d2h_bytes) / (hb + db)) * 1e3
+    return {"h2d_gbs": round(hb / t_up / 1e9, 1), "d2h_gbs": round(db / t_dn / 1e9, 1),
+            "both_gbs": round((hb + db) / t_both / 1e9, 1), "copy_floor_ms": round(floor_ms, 4)}
+
+
 # ---------------------------------------------------------------------------
 # Branches of one shared prefix: one call reading the prefix state in place vs restore + prefill per branch
 # ---------------------------------------------------------------------------
@@ -591,8 +669,9 @@ def cpu_threads(n_heads: int) -> int:
 # kernel kind -> (source file, committed ncu summary) of the bf16 path
 # kernel kind -> (the sources that define its code, its ncu summary); the summary's figures are used only
 # while the sha256 over those sources matches the one it records
-PROFILED = {"prep_wy": (("prep_umma.cu", "umma.cuh", "mma.cuh", "common.cuh"), "prep_umma_qwen08b_replay.md"),
-            "state_output": (("chain_tc.cu", "mma.cuh", "common.cuh"), "state_output_qwen08b_replay.md")}
+PROFILED = {"prep_wy": (("prep_umma.cu", "prologue_umma.cuh", "umma.cuh", "mma.cuh", "common.cuh"),
+                        "prep_umma_qwen08b_replay.md"),
+            "state_output": (("chain_tc.cu", "chain_tc.cuh", "mma.cuh", "common.cuh"), "state_output_qwen08b_replay.md")}
 
 
 def source_sha16(names) -> str:
@@ -704,9 +783,12 @@ def main():
         # the downloaded outputs are the device's, row for row
         assert torch.equal(step.host_out, step.out.cpu()), "host outputs differ from the device outputs"
         e2e = {"value": etok / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": step.h2d_bytes,
-               "d2h_bytes_per_step": step.d2h_bytes,
-               "copies": "each turn's new input rows uploaded on a copy stream ahead of the compute, each turn's "
-                         "output rows downloaded on another as soon as the turn is done"}
+               "d2h_bytes_per_step": step.d2h_bytes, "ms_per_step": round(ems / args.steps, 4)}
+        if hasattr(step, "n_copies"):
+            e2e["copies"] = (f"{step.n_copies} copies per step: gates and weights, then input rows by groups of "
+                             f"{step.up_group} calls on one copy stream ahead of the compute; output rows by groups "
+                             f"of {step.down_group} calls on another as soon as a group is done")
+        e2e["host_link"] = host_link_measure(step)
 
     # --- roofline of the dominant kernel ---
     sh = w.shape
