@@ -165,13 +165,7 @@ __device__ __forceinline__ void store_c16x8(float *Z, int lz, const float (&c)[4
 __device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        __nv_bfloat16 h0, l0, h1, l1;
-        split_bf16(v[2 * q], h0, l0);
-        split_bf16(v[2 * q + 1], h1, l1);
-        h[q] = pack_bf16(h0, h1);
-        l[q] = pack_bf16(l0, l1);
-    }
+    for (int q = 0; q < 4; ++q) split_bf16x2(v[2 * q], v[2 * q + 1], h[q], l[q]);
     hi = make_uint4(h[0], h[1], h[2], h[3]);
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
@@ -346,11 +340,11 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         }
     };
     auto split4_store = [&](unsigned char *hi, unsigned char *lo, uint32_t off, const float (&v)[4]) {
-        __nv_bfloat16 h[4], l[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) split_bf16(v[c], h[c], l[c]);
-        *reinterpret_cast<uint2 *>(hi + off) = make_uint2(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]));
-        *reinterpret_cast<uint2 *>(lo + off) = make_uint2(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]));
+        uint32_t h0, h1, l0, l1;
+        split_bf16x2(v[0], v[1], h0, l0);
+        split_bf16x2(v[2], v[3], h1, l1);
+        *reinterpret_cast<uint2 *>(hi + off) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2 *>(lo + off) = make_uint2(l0, l1);
     };
     auto store8 = [&](unsigned char *hi, unsigned char *lo, uint32_t off, const float *v) {
         uint4 h, l;
@@ -538,9 +532,13 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         __syncthreads();
 
         // 7. T = (I + A)^{-1} (unit lower triangular) in fp32, two levels of 2x2 blocking:
-        //    diagonal 16x16 blocks D_b by substitution (one column per thread; the other threads zero the
-        //    blocks above the diagonal), then T_10 = -D_1 A_10 D_0 and T_32 = -D_3 A_32 D_2, then
-        //    T[32:64, 0:32] = -T[32:64, 32:64] A[32:64, 0:32] T[0:32, 0:32]; products as split-tf32 MMAs
+        //    diagonal 16x16 blocks D_b by substitution (one column per thread, warp 0: D_0, D_1, warp 1: D_2,
+        //    D_3; the other threads zero the blocks above the diagonal), then on the same warps
+        //    T_10 = -D_1 A_10 D_0 and T_32 = -D_3 A_32 D_2, then T[32:64, 0:32] = -T[32:64, 32:64] A[32:64, 0:32]
+        //    T[0:32, 0:32] on warps 0-3, one 8-column tile each; products as split-tf32 MMAs. A warp reads only
+        //    what it wrote between the CTA barriers, so warp barriers order the steps within a level.
+        constexpr int LM = 24, LX = 40;
+        float *Xs = reinterpret_cast<float *>(TBh);   // 32 x LX scratch (the T operand regions are written later)
         if (t < kBlock) {
             const int d = t >> 4, c = t & 15;
             const float *Ad = Af + 16 * d * LT + 16 * d;
@@ -555,6 +553,22 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tf[(16 * d + i) * LT + 16 * d + c] = x[i];
+            __syncwarp();
+            const int b = 2 * warp;   // block pair (b + 1, b)
+            float *M = Mt + warp * 16 * LM;
+#pragma unroll 1
+            for (int nt = 0; nt < 2; ++nt) {
+                float cc[4] = {0.f, 0.f, 0.f, 0.f};
+                mma3_tf32_16x8(cc, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, 16, lane);
+                store_c16x8(M + 8 * nt, LM, cc, 1.f, lane);
+            }
+            __syncwarp();
+#pragma unroll 1
+            for (int nt = 0; nt < 2; ++nt) {
+                float cc[4] = {0.f, 0.f, 0.f, 0.f};
+                mma3_tf32_16x8(cc, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, M + 8 * nt, LM, 16, lane);
+                store_c16x8(Tf + 16 * (b + 1) * LT + 16 * b + 8 * nt, LT, cc, -1.f, lane);
+            }
         } else {
             for (int e = t - kBlock; e < 6 * 64; e += kUmmaPrepThreads - kBlock) {   // 6 blocks x 16 rows x 4 float4
                 const int bi = e >> 6, r = (e >> 2) & 15, c4 = e & 3;
@@ -563,34 +577,21 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             }
         }
         __syncthreads();
-        constexpr int LM = 24, LX = 40;
-        float *Xs = reinterpret_cast<float *>(TBh);   // 32 x LX scratch (the T operand regions are written later)
-        if (warp < 4) {   // warps 0,1: block pair (1, 0); warps 2,3: (3, 2); 8 columns each
-            const int b = 2 * (warp >> 1), nt = warp & 1;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            mma3_tf32_16x8(c, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, 16, lane);
-            store_c16x8(Mt + (warp >> 1) * 16 * LM + 8 * nt, LM, c, 1.f, lane);
-        }
-        __syncthreads();
-        if (warp < 4) {
-            const int b = 2 * (warp >> 1), nt = warp & 1;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            mma3_tf32_16x8(c, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, Mt + (warp >> 1) * 16 * LM + 8 * nt, LM, 16, lane);
-            store_c16x8(Tf + 16 * (b + 1) * LT + 16 * b + 8 * nt, LT, c, -1.f, lane);
-        }
-        __syncthreads();
-        if (warp < 8) {   // X = A[32:64, 0:32] T[0:32, 0:32]: 2 m-tiles x 4 n-tiles
-            const int mt = warp >> 2, nt = warp & 3;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            mma3_tf32_16x8(c, Af + (32 + 16 * mt) * LT, LT, Tf + 8 * nt, LT, 32, lane);
-            store_c16x8(Xs + 16 * mt * LX + 8 * nt, LX, c, 1.f, lane);
-        }
-        __syncthreads();
-        if (warp < 8) {   // T[32:64, 0:32] = -T[32:64, 32:64] X
-            const int mt = warp >> 2, nt = warp & 3;
-            float c[4] = {0.f, 0.f, 0.f, 0.f};
-            mma3_tf32_16x8(c, Tf + (32 + 16 * mt) * LT + 32, LT, Xs + 8 * nt, LX, 32, lane);
-            store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, c, -1.f, lane);
+        if (warp < 4) {   // column tile nt = warp: X = A[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] X
+            const int nt = warp;
+#pragma unroll 1
+            for (int mt = 0; mt < 2; ++mt) {
+                float cc[4] = {0.f, 0.f, 0.f, 0.f};
+                mma3_tf32_16x8(cc, Af + (32 + 16 * mt) * LT, LT, Tf + 8 * nt, LT, 32, lane);
+                store_c16x8(Xs + 16 * mt * LX + 8 * nt, LX, cc, 1.f, lane);
+            }
+            __syncwarp();
+#pragma unroll 1
+            for (int mt = 0; mt < 2; ++mt) {
+                float cc[4] = {0.f, 0.f, 0.f, 0.f};
+                mma3_tf32_16x8(cc, Tf + (32 + 16 * mt) * LT + 32, LT, Xs + 8 * nt, LX, 32, lane);
+                store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, cc, -1.f, lane);
+            }
         }
         __syncthreads();
         //    T as bf16 hi/lo: rows 0..63 of [T; P T] (K-major, written over A and T) and the B operand of
