@@ -15,14 +15,18 @@ __global__ void __launch_bounds__(kThreads, 1) chain_tc_kernel(const __grid_cons
     extern __shared__ __align__(16) float smem[];
     Chain<D, DS> c(p, smem, blockIdx.x);
     const int t = threadIdx.x, nb = c.nb;
+    grid_dep_launch();   // the next call's prologue may take SMs as this kernel's CTAs leave
+    if (t == 0) c.init_bars();
+    grid_dep_wait();     // the records of this call, the state and the conv state
+    if (t == 0) {   // the first block's copies go out first; the conv commit and the state load overlap them
+        if (nb > 0) {
+            c.issue(0);
+            if constexpr (Chain<D, DS>::kSplit) c.issue_wq(0);
+        }
+    }
     c.conv_commit(ch);
     c.load_state();
-    if (t == 0) c.init_bars();
     __syncthreads();
-    if (t == 0 && nb > 0) {
-        c.issue(0);
-        if constexpr (Chain<D, DS>::kSplit) c.issue_wq(0);
-    }
     int timed_out = 0;
     for (int b = 0; b < nb; ++b) {
         if (t == 0 && b + 1 < nb) c.issue(b + 1);   // the other stage was released at the end of step b-1
@@ -51,8 +55,8 @@ static cudaError_t launch(const LaunchCommon &p, int64_t ch, cudaStream_t st) {
     auto k = chain_tc_kernel<D, DS>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<p.n_sess * p.Hv * (D / DS), kThreads, smem, st>>>(p, ch);
-    return cudaGetLastError();
+    e = gdn_launch_pdl(k, p.n_sess * p.Hv * (D / DS), kThreads, smem, st, p, ch);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int D>

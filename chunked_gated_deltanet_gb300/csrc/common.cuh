@@ -83,6 +83,14 @@ __device__ __forceinline__ int find_session(const LaunchCommon &p, int blk) {
     return s;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running. grid_dep_launch() lets the next kernel start (its
+// CTAs take SMs as ours leave); grid_dep_wait() returns once every earlier kernel has completed and its
+// memory operations are visible, so it must precede any read of data earlier work wrote (and any write
+// earlier work may still read). Both are no-ops without a programmatic predecessor or successor.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // Causal conv of one channel over a 64-row block, fixed fma order (oldest tap first).
 // x_at(i) returns the raw input at block row i (i in [-3, n)), zero is used past n.
 template <typename InT>
@@ -104,6 +112,24 @@ cudaError_t gdn_device_error_word(unsigned int **out);
 
 // Number of SMs of the current device (looked up once per device).
 cudaError_t gdn_sm_count(int *out);
+
+// Launches kernel<<<grid, block, smem, st>>>(args...) with programmatic stream serialization (the kernel
+// calls grid_dep_wait before touching data of earlier work).
+template <class... K, class... A>
+cudaError_t gdn_launch_pdl(void (*kernel)(K...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                           A &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<A &&>(args)...);
+}
 
 // Sets the message gdn_last_error() returns on this host thread (library-internal).
 void gdn_internal_set_error(const char *msg);

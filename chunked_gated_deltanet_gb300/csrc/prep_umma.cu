@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tslot;
+    grid_dep_launch();   // the state kernel may take SMs as this kernel's CTAs leave
+    grid_dep_wait();     // inputs and conv state of this call, written by earlier work
     StridedTasks src{(int)blockIdx.x, p.nblk * p.Hk};
     prologue_run(p, ch, sm, ctl, tmem, src);
     tc_fence_after();
@@ -31,6 +33,6 @@ cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStr
     int sms = 1;   // one persistent CTA per SM (shared memory allows no more), over nblk x Hk tasks
     if ((e = gdn_sm_count(&sms)) != cudaSuccess) return e;
     const int ntask = p.nblk * p.Hk;
-    prep_umma_kernel<<<ntask < sms ? ntask : sms, kUmmaPrepThreads, up::SMEM, st>>>(p, ch);
-    return cudaGetLastError();
+    e = gdn_launch_pdl(prep_umma_kernel, ntask < sms ? ntask : sms, kUmmaPrepThreads, up::SMEM, st, p, ch);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
