@@ -827,7 +827,7 @@ def main():
                                  "frac": round(achieved_tf / tf32, 4)}}
     gpu_launches = int(sum(v[0] for v in ktimes.values()))
 
-    decode = None if args.no_decode else [decode_measure(w, dev, n) for n in (1, 64, 256)]
+    decode = None if args.no_decode else [decode_measure(w, dev, n) for n in (1, 256)]
     branches = None if args.no_decode else branches_measure(dev)
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
