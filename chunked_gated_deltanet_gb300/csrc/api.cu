@@ -163,8 +163,8 @@ cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int6
 }
 
 // ---- optional per-kernel event timing ----
-enum Kind { K_PREP = 0, K_CONV = 1, K_STATE = 2, K_COPY = 3, K_DECODE = 4, K_KINDS = 5 };
-const char *const kKindName[K_KINDS] = {"prep_wy", "conv_commit", "state_output", "state_copy", "decode"};
+enum Kind { K_PREP = 0, K_CONV = 1, K_STATE = 2, K_COPY = 3, K_DECODE = 4, K_GATES = 5, K_KINDS = 6 };
+const char *const kKindName[K_KINDS] = {"prep_wy", "conv_commit", "state_output", "state_copy", "decode", "gates"};
 
 struct Timing {
     bool on = false;
@@ -582,6 +582,25 @@ GDN_API gdn_status gdn_decode_step(const gdn_layer_desc *d, gdn_session *session
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
     }
     for (int i = 0; i < n; ++i) sessions[i].committed += 1;
+    return GDN_OK;
+}
+
+GDN_API gdn_status gdn_gates(const gdn_layer_desc *d, const float *a, const float *b, const float *A_log,
+                             const float *dt_bias, int64_t n_tokens, float *g, float *beta, gdn_stream_t stream) {
+    gdn_status st = check_desc(d);
+    if (st != GDN_OK) return st;
+    if (n_tokens < 0 || n_tokens > ((int64_t)1 << 40) / d->n_v_heads)
+        return fail(GDN_ERR_INVALID_ARG, "n_tokens out of range (%lld)", (long long)n_tokens);
+    if (!a || !b || !A_log || !dt_bias || !g || !beta)
+        return fail(GDN_ERR_INVALID_ARG, "a, b, A_log, dt_bias, g, beta must be non-NULL");
+    for (const void *q : {(const void *)a, (const void *)b, (const void *)A_log, (const void *)dt_bias,
+                          (const void *)g, (const void *)beta})
+        if (reinterpret_cast<uintptr_t>(q) & 3) return fail(GDN_ERR_INVALID_ARG, "gate arrays must be 4-byte aligned");
+    cudaStream_t cst = (cudaStream_t)stream;
+    cudaError_t e = launch_k(K_GATES, cst, [&] {
+        return gdn_launch_gates(a, b, A_log, dt_bias, n_tokens * d->n_v_heads, d->n_v_heads, g, beta, cst);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "gate kernel");
     return GDN_OK;
 }
 

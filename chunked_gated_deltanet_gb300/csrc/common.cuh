@@ -144,3 +144,5 @@ cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf1
 cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *dst1, const void *src1,
                             size_t bytes1, cudaStream_t st);
 cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
+cudaError_t gdn_launch_gates(const float *a, const float *b, const float *A_log, const float *dt_bias, int64_t n,
+                             int Hv, float *g, float *beta, cudaStream_t st);

@@ -1,5 +1,7 @@
 // Conv-state commit, state copy (checkpoint capture / restore, session zeroing)
 // and the one-token decode step (which commits its own conv state).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace gdn {
@@ -161,7 +163,30 @@ __global__ void __launch_bounds__(256) decode_kernel(const LaunchCommon p, int64
     }
 }
 
+// g and beta from raw per-token projections (the raw-gate variant, the usual Gated-DeltaNet
+// parametrisation; the pages take g and beta as given):
+//   g = -exp(A_log[h]) * softplus(a + dt_bias[h]),  beta = 1 / (1 + exp(-b)),
+// softplus(x) = max(x, 0) + log1p(exp(-|x|)), element i of [tokens][Hv] belonging to head i % Hv.
+__global__ void __launch_bounds__(256) gates_kernel(const float *a, const float *b, const float *A_log,
+                                                    const float *dt_bias, int64_t n, int Hv, float *g, float *beta) {
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256) {
+        const int h = (int)(i % Hv);
+        const float x = a[i] + dt_bias[h];
+        const float sp = fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
+        g[i] = -expf(A_log[h]) * sp;
+        beta[i] = 1.f / (1.f + expf(-b[i]));
+    }
+}
+
 }  // namespace gdn
+
+cudaError_t gdn_launch_gates(const float *a, const float *b, const float *A_log, const float *dt_bias, int64_t n,
+                             int Hv, float *g, float *beta, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 8);
+    gdn::gates_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, b, A_log, dt_bias, n, Hv, g, beta);
+    return cudaGetLastError();
+}
 
 cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st) {
     using namespace gdn;

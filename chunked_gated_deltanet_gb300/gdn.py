@@ -35,7 +35,7 @@ GDN_MAX_SESSIONS = 4096
 EXPORTED = ["gdn_desc_tag", "gdn_desc_check", "gdn_state_bytes", "gdn_conv_state_bytes", "gdn_session_init",
             "gdn_workspace_size", "gdn_prefill_chunks", "gdn_prefill_varlen", "gdn_state_capture",
             "gdn_state_restore", "gdn_conv_state", "gdn_decode_step", "gdn_timing_begin", "gdn_timing_end",
-            "gdn_prefill_chunks_noalloc", "gdn_device_status", "gdn_debug_inject_wait_timeout",
+            "gdn_prefill_chunks_noalloc", "gdn_device_status", "gdn_debug_inject_wait_timeout", "gdn_gates",
             "gdn_last_error", "gdn_status_string", "gdn_state_blob_bytes", "gdn_state_serialize",
             "gdn_state_deserialize", "gdn_state_save", "gdn_state_load", "gdn_prefill_branches",
             "gdn_prefill_chunks_checkpoint", "gdn_prefill_varlen_checkpoint"]
@@ -106,6 +106,7 @@ def load_library(path: Optional[str] = None):
         "gdn_timing_end": (ctypes.c_int, [ctypes.POINTER(gdn_kernel_time), i32, ctypes.POINTER(i32)]),
         "gdn_device_status": (ctypes.c_int, [vp]),
         "gdn_debug_inject_wait_timeout": (ctypes.c_int, [i32, i64]),
+        "gdn_gates": (ctypes.c_int, [D, vp, vp, vp, vp, i64, vp, vp, vp]),
         "gdn_last_error": (ctypes.c_char_p, []),
         "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "gdn_state_blob_bytes": (ctypes.c_size_t, [D]),
@@ -324,6 +325,20 @@ def gdn_decode_step(desc, sessions: Sequence[Session], xq, xk, xv, g, beta, conv
     for i, s in enumerate(sessions):
         s.c.committed = arr[i].committed
     _check(st)
+
+
+def gdn_gates(desc, a: torch.Tensor, b: torch.Tensor, A_log: torch.Tensor, dt_bias: torch.Tensor,
+              g: torch.Tensor, beta: torch.Tensor, stream=None):
+    """g, beta [n][Hv] from raw projections a, b [n][Hv] and per-head A_log, dt_bias [Hv] (fp32, on the GPU)."""
+    n = a.shape[0]
+    for t in (a, b, g, beta):
+        if t.dtype != torch.float32 or tuple(t.shape) != (n, desc.n_v_heads):
+            raise ValueError("a, b, g, beta must be fp32 [n_tokens][n_v_heads]")
+    for t in (A_log, dt_bias):
+        if t.dtype != torch.float32 or t.numel() != desc.n_v_heads:
+            raise ValueError("A_log, dt_bias must be fp32 [n_v_heads]")
+    _check(load_library().gdn_gates(ctypes.byref(desc), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), n, _ptr(g),
+                                    _ptr(beta), _stream(stream)))
 
 
 def gdn_state_blob_bytes(desc) -> int:

@@ -16,6 +16,10 @@ stand in for them, with the shapes of those workloads:
   (mu = 0, scale = 0.1 by default; the long-session workload uses mu = -2,
   scale = 1).
 * conv weights ~ N(0, 0.5^2), kernel 4, rounded to the input dtype.
+* raw-gate inputs (the optional variant that computes g and beta from
+  projections): a ~ N(0, 1), b ~ N(0, 1) per token and v-head; per head
+  A_log = ln U(0.05, 0.5) and dt_bias ~ N(-2, 0.5), so that the resulting
+  log-decays stay moderate (about -0.5 to -0.003), like the drawn g above.
 
 All draws use numpy's PCG64 through independent SeedSequence streams:
 stream (seed, 0) for layer weights, (seed, 1 + i) for session i's tokens,
@@ -174,6 +178,16 @@ def draw_tokens(shape: Shape, T: int, seed: int, stream: int, g_mu: float = 0.0,
 # ---------------------------------------------------------------------------
 # Turn / length recipes
 # ---------------------------------------------------------------------------
+
+def draw_raw_gates(T: int, n_v_heads: int, seed: int):
+    """Raw-gate inputs (fp32): a, b [T, Hv] and per-head A_log, dt_bias [Hv]; stream (seed, 20_000)."""
+    rng = _rng(seed, 20_000)
+    a = rng.standard_normal((T, n_v_heads)).astype(np.float32)
+    b = rng.standard_normal((T, n_v_heads)).astype(np.float32)
+    A_log = np.log(rng.uniform(0.05, 0.5, n_v_heads)).astype(np.float32)
+    dt_bias = rng.normal(-2.0, 0.5, n_v_heads).astype(np.float32)
+    return a, b, A_log, dt_bias
+
 
 def split_turns(total: int, n_turns: int, rng: np.random.Generator, lo: int = 0,
                 hi: Optional[int] = None, max_tries: int = 100000) -> List[int]:

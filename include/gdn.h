@@ -286,6 +286,18 @@ gdn_status gdn_decode_step(const gdn_layer_desc *desc, gdn_session *sessions, in
                            const void *xq, const void *xk, const void *xv, const float *g,
                            const float *beta, const void *conv_w, void *out, gdn_stream_t stream);
 
+/* Raw-gate inputs: g and beta of every token from its raw projections, on the
+ * GPU, for the prefill and decode calls above (which take g and beta as given,
+ * the form the pages use). The parametrisation is the usual one of
+ * Gated-DeltaNet layers, a reading outside the pages: per token t and v-head h,
+ *   g[t][h]    = -exp(A_log[h]) * softplus(a[t][h] + dt_bias[h]),
+ *   beta[t][h] = 1 / (1 + exp(-b[t][h])),   softplus(x) = log(1 + exp(x)).
+ * a, b, g, beta: fp32 device [n_tokens][Hv]; A_log, dt_bias: fp32 device [Hv]
+ * (4-byte aligned). g and beta may be the same buffers as a and b. Stream-
+ * ordered; errors as for the prefill calls. */
+gdn_status gdn_gates(const gdn_layer_desc *desc, const float *a, const float *b, const float *A_log,
+                     const float *dt_bias, int64_t n_tokens, float *g, float *beta, gdn_stream_t stream);
+
 /* Per-kernel timing with CUDA events, for benchmarks (off by default).
  * gdn_timing_begin(max_launches) creates 2 * max_launches events and starts
  * recording: every kernel the library launches afterwards, on whatever stream
@@ -296,7 +308,7 @@ gdn_status gdn_decode_step(const gdn_layer_desc *desc, gdn_session *sessions, in
  * with *n_kinds the number of kinds that launched. Process-global and not
  * thread-safe: one benchmark thread at a time. */
 typedef struct gdn_kernel_time {
-    char name[32];        /* kernel kind: prep_wy, conv_commit, state_output, state_copy, decode */
+    char name[32];        /* kernel kind: prep_wy, conv_commit, state_output, state_copy, decode, gates */
     int64_t launches;     /* launches while recording */
     int64_t timed;        /* launches with an event pair */
     double total_ms;      /* summed device time of the timed launches */

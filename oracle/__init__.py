@@ -5,7 +5,8 @@ baseline may import this package; the library and its Python binding never do.
 It shares no code with the CUDA path.
 
 Contents
-  gdn_oracle.c   conv + L2 norm + the token-by-token gated delta rule in fp64 (C)
+  gdn_oracle.c   conv + L2 norm + the token-by-token gated delta rule in fp64 (C),
+                 and the raw-gate variant's g and beta from projections
   chunked.py     the chunked (WY / UT) form in fp64 numpy, used only to check
                  the algebraic identity with the recurrence
   brute.py       exact rational brute force of the recurrence for tiny inputs
@@ -48,6 +49,8 @@ def _load():
         lib.oracle_layer.argtypes = [i64, ci, ci, ci, ci, ci, ctypes.c_double, ctypes.c_double,
                                      d, d, d, d, d, d, d, d, d]
         lib.oracle_layer.restype = ctypes.c_int
+        lib.oracle_gates.argtypes = [i64, ci, d, d, d, d, d, d]
+        lib.oracle_gates.restype = None
         _lib = lib
     return _lib
 
@@ -115,6 +118,19 @@ def layer(xq, xk, xv, g, beta, conv_w, Hk: int, Hv: int, conv_state=None, ST0=No
     if rc != 0:
         raise RuntimeError(f"oracle_layer failed ({rc})")
     return o, ST, cs
+
+
+def gates(a, b, A_log, dt_bias):
+    """g and beta from raw projections (the raw-gate variant, a reading outside the pages: the usual
+    Gated-DeltaNet parametrisation g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)).
+
+    a, b: [T, Hv]; A_log, dt_bias: [Hv]. Returns (g, beta), each [T, Hv]."""
+    a, b, A_log, dt_bias = map(_c, (a, b, A_log, dt_bias))
+    T, Hv = a.shape
+    g = np.zeros((T, Hv))
+    beta = np.zeros((T, Hv))
+    _load().oracle_gates(T, Hv, _p(a), _p(b), _p(A_log), _p(dt_bias), _p(g), _p(beta))
+    return g, beta
 
 
 def head_columns(Hk: int, Hv: int, dk: int, dv: int, v_heads: Sequence[int]):

@@ -169,3 +169,25 @@ EXPORT int oracle_layer(int64_t T, int Hk, int Hv, int dk, int dv, int act,
     free(yq); free(yk); free(yv); free(st); free(st_out); free(a);
     return 0;
 }
+
+/*
+ * Gates from raw per-token projections (the optional raw-gate variant). The
+ * pages take g and beta as given, already activated; this variant follows the
+ * usual Gated-DeltaNet parametrisation of such layers (a reading, not in the
+ * pages): per token t and v-head h,
+ *   g[t][h]    = -exp(A_log[h]) * softplus(a[t][h] + dt_bias[h]),
+ *   beta[t][h] = 1 / (1 + exp(-b[t][h])),
+ * with softplus(x) = log(1 + exp(x)), evaluated as max(x, 0) + log1p(exp(-|x|))
+ * (the same function, without overflow for large x).
+ */
+EXPORT void oracle_gates(int64_t T, int Hv, const double *a, const double *b, const double *A_log,
+                  const double *dt_bias, double *g, double *beta) {
+    for (int64_t t = 0; t < T; ++t)
+        for (int h = 0; h < Hv; ++h) {
+            const int64_t i = t * Hv + h;
+            const double x = a[i] + dt_bias[h];
+            const double sp = (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+            g[i] = -exp(A_log[h]) * sp;
+            beta[i] = 1.0 / (1.0 + exp(-b[i]));
+        }
+}

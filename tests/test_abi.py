@@ -206,3 +206,18 @@ def test_branch_and_checkpoint_refusals(lib):
     assert lib.gdn_prefill_varlen_checkpoint(ctypes.byref(d), ctypes.byref(s), None, 1, cu, *x[:6], 0, x[6], nc,
                                              vp(0x9000000), 1 << 30, None) == gdn.GDN_ERR_INVALID_ARG
     assert (slot.committed, s.committed) == (-1, 0)
+
+
+def test_gate_call_refusals(lib):
+    """gdn_gates checks its layer description, sizes, pointers and alignment on the host."""
+    d = gdn.make_desc(2, 4, 64, 64, 64)
+    P = lambda v: ctypes.c_void_p(v)
+    ok = [P(0x1000), P(0x2000), P(0x3000), P(0x4000)]
+    outs = [P(0x5000), P(0x6000)]
+    call = lambda desc, ins, n, o: lib.gdn_gates(ctypes.byref(desc), *ins, n, *o, None)
+    assert call(d, [None] + ok[1:], 8, outs) == gdn.GDN_ERR_INVALID_ARG
+    assert call(d, ok, 8, [outs[0], None]) == gdn.GDN_ERR_INVALID_ARG
+    assert call(d, [P(0x1002)] + ok[1:], 8, outs) == gdn.GDN_ERR_INVALID_ARG     # misaligned
+    assert call(d, ok, -1, outs) == gdn.GDN_ERR_INVALID_ARG
+    bad = gdn.make_desc(2, 3, 64, 64, 64)                                      # Hv not a multiple of Hk
+    assert call(bad, ok, 8, outs) != gdn.GDN_OK

@@ -304,3 +304,28 @@ def test_layer_split_invariance():
         ob, STb, csb = oracle.layer(Hk=Hk, Hv=Hv, conv_state=csa, ST0=STa, **p2)
         assert np.array_equal(np.concatenate([oa, ob]), o)
         assert np.array_equal(STb, ST) and np.array_equal(csb, cs)
+
+
+def test_gates_closed_forms():
+    """The raw-gate variant's g = -exp(A_log) softplus(a + dt_bias) and beta = sigmoid(b), pinned by values
+    known in closed form: softplus(0) = ln 2, softplus(ln(e - 1)) = 1, softplus(x) -> x for large x and
+    -> e^x for very negative x; sigmoid(0) = 1/2, sigmoid(+-ln 3) = 3/4, 1/4. Two heads with different
+    parameters pin the per-head indexing."""
+    L3 = np.log(3.0)
+    a = np.array([[0.0 - 0.25, np.log(np.e - 1.0)],     # head 0: x = a + dt_bias = 0
+                  [50.0 - 0.25, -50.0],
+                  [-0.25, 0.0]])
+    b = np.array([[0.0, L3], [-L3, 0.0], [L3, -L3]])
+    A_log = np.array([L3, 0.0])                          # exp(A_log) = 3, 1
+    dt_bias = np.array([0.25, 0.0])
+    g, beta = oracle.gates(a, b, A_log, dt_bias)
+    assert g[0, 0] == pytest.approx(-3.0 * np.log(2.0), rel=1e-15)
+    assert g[0, 1] == pytest.approx(-1.0, rel=1e-15)
+    assert g[1, 0] == pytest.approx(-3.0 * 50.0, rel=1e-15)
+    assert g[1, 1] == pytest.approx(-np.exp(-50.0), rel=1e-12)
+    assert g[2, 0] == pytest.approx(-3.0 * np.log(2.0), rel=1e-15)
+    assert g[2, 1] == pytest.approx(-np.log(2.0), rel=1e-15)
+    assert np.all(g < 0)
+    assert beta[0, 0] == 0.5 and beta[1, 1] == 0.5
+    assert beta[0, 1] == pytest.approx(0.75, rel=1e-15) and beta[2, 0] == pytest.approx(0.75, rel=1e-15)
+    assert beta[1, 0] == pytest.approx(0.25, rel=1e-15) and beta[2, 1] == pytest.approx(0.25, rel=1e-15)
