@@ -132,6 +132,7 @@ int g_skip_first_copy = 0;
 void fill_common(LaunchCommon &p, const gdn_layer_desc *d, const void *xq, const void *xk, const void *xv,
                  const float *g, const float *beta, const void *conv_w, void *out) {
     std::memset(&p, 0, sizeof(p));
+    for (int i = 0; i < gdn::kLaunchSessions; ++i) p.order[i] = (unsigned char)i;
     p.wait_limit = g_wait_limit;
     p.debug_skip_first_copy = g_skip_first_copy;
     p.xq = xq; p.xk = xk; p.xv = xv; p.g = g; p.beta = beta; p.conv_w = conv_w; p.out = out;
@@ -393,6 +394,12 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
             i0 = i;
             if (cnt == 0) continue;
             p.n_sess = cnt; p.nblk = blk;
+            {   // the state kernel starts the longest chains first
+                int ord[gdn::kLaunchSessions];
+                for (int j = 0; j < cnt; ++j) ord[j] = j;
+                std::stable_sort(ord, ord + cnt, [&](int x, int y) { return p.s[x].n > p.s[y].n; });
+                for (int j = 0; j < cnt; ++j) p.order[j] = (unsigned char)ord[j];
+            }
             cudaError_t e = gdn_device_error_word(&p.err);
             if (e != cudaSuccess) return cuda_fail(e, "device error word lookup");
             if (in_bf16) {

@@ -58,7 +58,7 @@ struct Chain {
     bool owner;      // this warp owns state rows 16w..16w+15
     float st[NT][4]; // the state rows of this thread (accumulator layout)
 
-    // chain index cidx = ((session * Hv) + v-head) * (D / DS) + slice
+    // chain index cidx = ((rank * Hv) + v-head) * (D / DS) + slice, session p.order[rank]
     __device__ __forceinline__ Chain(const LaunchCommon &p_, float *smem_, int cidx) : p(p_), smem(smem_) {
         wqbuf = smem + 2 * STAGE;
         St = wqbuf + P::WQBUF;
@@ -66,7 +66,7 @@ struct Chain {
         bar = reinterpret_cast<uint64_t *>(Ups + kBlock * SP);
         sl = cidx % nsl;
         h = (cidx / nsl) % p.Hv;
-        s = p.s[cidx / (nsl * p.Hv)];
+        s = p.s[p.order[cidx / (nsl * p.Hv)]];
         c0 = sl * DS;
         t = threadIdx.x; warp = t >> 5; lane = t & 31; g8 = lane >> 2; t4 = lane & 3;
         nb = (s.n + kBlock - 1) / kBlock;

@@ -41,6 +41,9 @@ struct LaunchCommon {
     unsigned int *err;          // device error word (bit 0: a bounded wait ran out)
     int debug_skip_first_copy;  // test hook: 1 = the state kernel, 2 = the tcgen05 prologue never issues its first copy
     SessRef s[kLaunchSessions];
+    // the state kernel's session order: chain CTAs are numbered session order[0] first (the caller lists
+    // the longest first, so that the longest chains start first and the launch packs well)
+    unsigned char order[kLaunchSessions];
     // 2-D tensor maps over xq [rows][Hk D], xk [rows][Hk D], xv [rows][Hv D] (bf16, boxes of 64 rows x 128
     // channels) for the tcgen05 prologue's input copies; encoded by the host per call, unused elsewhere
     CUtensorMap tm_q, tm_k, tm_v;
