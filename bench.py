@@ -270,10 +270,11 @@ class ReplayStep:
                              flags=g.GDN_ALLOW_PARTIAL)
         g.gdn_state_restore(d, s, slot)
 
-    # call groups of the end-to-end copies (calls per copy; chosen by a sweep on the GB300 machine: 4 calls per
-    # upload and 2 per download gave the shortest step, about 10 % below one copy per call and tensor)
-    up_group = 4
-    down_group = 2
+    # call groups of the end-to-end copies (calls per copy; chosen by a sweep on the GB300 machine with the two
+    # buffer sets: 8 calls per upload and 4 per download gave the shortest step, 2.998 ms against 3.17 ms
+    # for 2 and 2 or for one copy per tensor of the whole step)
+    up_group = 8
+    down_group = 4
 
     def up_sizes(self, n):
         return [self.up_group] * (-(-n // self.up_group))
@@ -285,13 +286,15 @@ class ReplayStep:
         """Copy plan of the end-to-end step. Every copy costs a few microseconds of idle host link, so inputs
         go up in fewer, larger copies: the gates and conv weights of the whole step first, then the q/k/v rows
         of groups of calls (a call waits only for its group); outputs come down by groups of calls. Groups
-        that are too large make the compute wait for the link. Raw pointers, two copy streams and the events
-        that order them."""
+        that are too large make the compute wait for the link. Two sets of device buffers take turns, so
+        that the next step's inputs go up while this step computes, as in a serving loop; a set is refilled
+        once the compute of the step before last no longer reads it, and its outputs are overwritten once
+        their download is done. Raw pointers, two copy streams and the events that order them."""
         torch = self.torch
         self.rt = CudaRuntime()
         self.h2d, self.d2h = torch.cuda.Stream(), torch.cuda.Stream()
-        row_bytes = [(t.stride(0) * t.element_size(), d.data_ptr(), t.data_ptr()) for d, t in zip(self.x, self.host)]
-        out_row = self.out.stride(0) * self.out.element_size()
+        self.sets = [(self.x, self.cw, self.out),
+                     ([torch.empty_like(t) for t in self.x], torch.empty_like(self.cw), torch.empty_like(self.out))]
         spans = [(a, b, take) for a, b, take in self.calls] + [(self.fork[0], self.fork[1], self.fork[1] - self.fork[0])]
         n = len(spans)
 
@@ -306,56 +309,81 @@ class ReplayStep:
                 out.append((k, n))
             return out
 
-        # uploads: whole-step gates and weights, then q, k, v rows by call group
-        self.up_first = [(rb_dp_hp[1], rb_dp_hp[2], self.rows * rb_dp_hp[0]) for rb_dp_hp in row_bytes[3:]]
-        self.up_first.append((self.cw.data_ptr(), self.host_cw.data_ptr(), self.cw.numel() * self.cw.element_size()))
-        self.up_groups, self.up_of = [], [0] * n
-        for gi, (k0, k1) in enumerate(groups(self.up_sizes(n))):
-            r0 = spans[k0 - 1][1] if k0 > 0 else 0
-            r1 = spans[k1 - 1][1]
-            self.up_groups.append([(dp + r0 * rb, hp + r0 * rb, (r1 - r0) * rb) for rb, dp, hp in row_bytes[:3]])
+        up_groups, self.up_of = groups(self.up_sizes(n)), [0] * n
+        for gi, (k0, k1) in enumerate(up_groups):
             for k in range(k0, k1):
                 self.up_of[k] = gi
-        # downloads: committed output rows by call group, issued after the group's last call
-        self.down_after = {}
-        for k0, k1 in groups(self.down_sizes(n)):
-            r0, r1 = spans[k0][0], spans[k1 - 1][0] + spans[k1 - 1][2]
-            self.down_after[k1 - 1] = (self.host_out.data_ptr() + r0 * out_row, self.out.data_ptr() + r0 * out_row,
-                                       (r1 - r0) * out_row)
-        self.n_copies = len(self.up_first) + 3 * len(self.up_groups) + len(self.down_after)
-        self.ev = [self.rt.event() for _ in range(len(self.up_groups) + n + 4)]
+        down_groups = groups(self.down_sizes(n))
+        self.plans = []
+        for x, cw, out in self.sets:
+            row_bytes = [(t.stride(0) * t.element_size(), d.data_ptr(), t.data_ptr()) for d, t in zip(x, self.host)]
+            out_row = out.stride(0) * out.element_size()
+            # uploads: whole-step gates and weights, then q, k, v rows by call group
+            first = [(dp, hp, self.rows * rb) for rb, dp, hp in row_bytes[3:]]
+            first.append((cw.data_ptr(), self.host_cw.data_ptr(), cw.numel() * cw.element_size()))
+            ups = []
+            for k0, k1 in up_groups:
+                r0 = spans[k0 - 1][1] if k0 > 0 else 0
+                r1 = spans[k1 - 1][1]
+                ups.append([(dp + r0 * rb, hp + r0 * rb, (r1 - r0) * rb) for rb, dp, hp in row_bytes[:3]])
+            # downloads: committed output rows by call group, issued after the group's last call
+            downs = {}
+            for k0, k1 in down_groups:
+                r0, r1 = spans[k0][0], spans[k1 - 1][0] + spans[k1 - 1][2]
+                downs[k1 - 1] = (self.host_out.data_ptr() + r0 * out_row, out.data_ptr() + r0 * out_row,
+                                 (r1 - r0) * out_row)
+            ev = {"up": [self.rt.event() for _ in ups], "call": [self.rt.event() for _ in range(n)],
+                  "in_free": self.rt.event(), "out_free": self.rt.event()}
+            self.plans.append((first, ups, downs, ev))
+        self.n_copies = len(self.plans[0][0]) + 3 * len(self.plans[0][1]) + len(self.plans[0][2])
+        self.gate_ev = self.rt.event()
+        self.k_e2e = 0
+
+    def e2e_gate(self, steps: int = 2):
+        """The uploads of the next `steps` steps wait for the compute stream's current position (the start
+        of a timed region), so that none of their copies runs before it."""
+        if not hasattr(self, "plans"):
+            self._e2e_setup()
+        self.rt.record(self.gate_ev, self.torch.cuda.current_stream().cuda_stream)
+        self.gate_left = steps
 
     def e2e_step(self):
-        """The step through host buffers: inputs go up on a copy stream ahead of the compute (each call waits
-        for the upload group that holds its rows), outputs come back on another copy stream by call group.
-        The compute stream waits for the last download, so every copy is inside the caller's timed region."""
+        """The step through host buffers on the next set of device buffers: inputs go up on a copy stream
+        ahead of the compute (each call waits for the upload group that holds its rows), outputs come back
+        on another copy stream by call group. e2e_finish() makes the compute stream wait for the outstanding
+        downloads."""
         g, torch = self.gdn, self.torch
-        if not hasattr(self, "up_groups"):
+        if not hasattr(self, "plans"):
             self._e2e_setup()
-        rt, ev = self.rt, self.ev
+        rt = self.rt
+        si = self.k_e2e % 2
+        self.k_e2e += 1
+        (x, cw, out), (first, ups, downs, ev) = self.sets[si], self.plans[si]
         comp = torch.cuda.current_stream().cuda_stream
         h2d, d2h = self.h2d.cuda_stream, self.d2h.cuda_stream
-        rt.record(ev[-1], comp)
-        rt.wait(h2d, ev[-1])                 # the previous step no longer reads the device inputs
-        for dst, src, nb in self.up_first:
+        if getattr(self, "gate_left", 0) > 0:
+            rt.wait(h2d, self.gate_ev)
+            self.gate_left -= 1
+        rt.wait(h2d, ev["in_free"])          # the step before last no longer reads this set's inputs
+        for dst, src, nb in first:
             rt.h2d(dst, src, nb, h2d)
-        for gi, grp in enumerate(self.up_groups):
+        for gi, grp in enumerate(ups):
             for dst, src, nb in grp:
                 rt.h2d(dst, src, nb, h2d)
-            rt.record(ev[gi], h2d)
-        d, s, x, cw, out, ws = self.desc, self.sess, self.x, self.cw, self.out, self.ws
-        nG = len(self.up_groups)
+            rt.record(ev["up"][gi], h2d)
+        rt.wait(comp, ev["out_free"])        # this set's outputs of the step before last are downloaded
+        d, s, ws = self.desc, self.sess, self.ws
 
         def after(k):
-            spec = self.down_after.get(k)
+            spec = downs.get(k)
             if spec is not None:
-                rt.record(ev[nG + k], comp)
-                rt.wait(d2h, ev[nG + k])
+                rt.record(ev["call"][k], comp)
+                rt.wait(d2h, ev["call"][k])
                 rt.d2h(*spec, d2h)
 
         g.gdn_session_init(d, s)
         for k, (a, b, take) in enumerate(self.calls):
-            rt.wait(comp, ev[self.up_of[k]])
+            rt.wait(comp, ev["up"][self.up_of[k]])
             slot = self.slots[k % len(self.slots)]
             n = g.gdn_prefill_chunks_checkpoint(d, s, slot, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b],
                                                 cw, out[a:b], ws)
@@ -363,13 +391,20 @@ class ReplayStep:
             after(k)
         a, b = self.fork
         k = len(self.calls)
-        rt.wait(comp, ev[self.up_of[k]])
+        rt.wait(comp, ev["up"][self.up_of[k]])
         g.gdn_prefill_chunks(d, s, x[0][a:b], x[1][a:b], x[2][a:b], x[3][a:b], x[4][a:b], cw, out[a:b], ws,
                              flags=g.GDN_ALLOW_PARTIAL)
         g.gdn_state_restore(d, s, slot)
+        rt.record(ev["in_free"], comp)
         after(k)
-        rt.record(ev[-2], d2h)
-        rt.wait(comp, ev[-2])
+        rt.record(ev["out_free"], d2h)
+        self.last_out = out
+
+    def e2e_finish(self):
+        """The compute stream waits for every download issued so far."""
+        comp = self.torch.cuda.current_stream().cuda_stream
+        for _, _, _, ev in self.plans:
+            self.rt.wait(comp, ev["out_free"])
 
     def config(self):
         sh = self.w.shape
@@ -770,24 +805,28 @@ def main():
     if not args.no_e2e:
         for _ in range(2):
             step.e2e_step()
+        step.e2e_finish()
         torch.cuda.synchronize()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        step.e2e_gate(2)   # the first two steps' uploads start inside the timed region
         for _ in range(args.steps):
             step.e2e_step()
+        step.e2e_finish()
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
         ems, etok = reduce_max_sum(e0.elapsed_time(e1), step.tokens_per_step * args.steps)
         # the downloaded outputs are the device's, row for row
-        assert torch.equal(step.host_out, step.out.cpu()), "host outputs differ from the device outputs"
+        assert torch.equal(step.host_out, step.last_out.cpu()), "host outputs differ from the device outputs"
         e2e = {"value": etok / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": step.h2d_bytes,
                "d2h_bytes_per_step": step.d2h_bytes, "ms_per_step": round(ems / args.steps, 4)}
         if hasattr(step, "n_copies"):
             e2e["copies"] = (f"{step.n_copies} copies per step: gates and weights, then input rows by groups of "
                              f"{step.up_group} calls on one copy stream ahead of the compute; output rows by groups "
-                             f"of {step.down_group} calls on another as soon as a group is done")
+                             f"of {step.down_group} calls on another as soon as a group is done; two sets of device "
+                             "buffers take turns, so the next step's inputs go up while this step computes")
         e2e["host_link"] = host_link_measure(step)
 
     # --- roofline of the dominant kernel ---
