@@ -693,6 +693,45 @@ def oracle_sample(w, n_tokens: int):
     return run
 
 
+def oracle_one_thread() -> dict:
+    """The oracle on one host thread (measured in a child process started with OMP_NUM_THREADS=1): the
+    2,048-token fp32 layer (2 heads, d = 64) whole, and one v-head of the 41,802-token replay session's
+    first 41,472 tokens."""
+    import numpy as np
+    import oracle
+    from chunked_gated_deltanet_gb300 import workloads as wl
+    out = {}
+    w = wl.small_fp32()
+    t0 = time.time()
+    oracle_sample(w, w.session_lengths[0])()
+    dt = time.time() - t0
+    out["fp32_T2048_H2_d64"] = {"tokens_per_s": round(w.session_lengths[0] / dt, 1), "seconds": round(dt, 3)}
+    w = wl.qwen08b_replay()
+    sh = w.shape
+    n = wl.grid_floor(w.session_lengths[0], sh.grid_c)
+    tok = w.session_tokens(0).slice(0, n)
+    k_heads, qk_cols, v_cols = oracle.head_columns(sh.n_qk_heads, sh.n_v_heads, sh.d_k, sh.d_v, [0])
+    f = lambda a: wl.as_f64(a, sh.dtype)
+    cw = w.conv_weights()
+    chan = np.concatenate([qk_cols, sh.n_qk_heads * sh.d_k + qk_cols, 2 * sh.n_qk_heads * sh.d_k + v_cols])
+    t0 = time.time()
+    oracle.layer(f(tok.xq[:, qk_cols]), f(tok.xk[:, qk_cols]), f(tok.xv[:, v_cols]), tok.g[:, [0]].astype(np.float64),
+                 tok.beta[:, [0]].astype(np.float64), f(cw[chan]), 1, 1)
+    dt = time.time() - t0
+    out["replay_one_head"] = {"tokens_per_s": round(n / dt, 1), "seconds": round(dt, 3), "tokens": n}
+    return out
+
+
+def oracle_one_thread_child():
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-one-thread"], env=env,
+                           capture_output=True, text=True, timeout=300, cwd=ROOT)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+    except Exception:
+        return None
+
+
 def cpu_threads(n_heads: int) -> int:
     try:
         c = len(os.sched_getaffinity(0))
@@ -701,7 +740,6 @@ def cpu_threads(n_heads: int) -> int:
     return max(1, min(c, n_heads))
 
 
-# kernel kind -> (source file, committed ncu summary) of the bf16 path
 # kernel kind -> (the sources that define its code, its ncu summary); the summary's figures are used only
 # while the sha256 over those sources matches the one it records
 PROFILED = {"prep_wy": (("prep_umma.cu", "prologue_umma.cuh", "umma.cuh", "mma.cuh", "common.cuh"),
@@ -746,10 +784,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode and branch measurements")
     ap.add_argument("--cpu-sample-tokens", type=int, default=41472)
+    ap.add_argument("--oracle-one-thread", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--workload", choices=["replay", "varlen8", "long_session"], default="replay",
                     help="replay: the headline (default); varlen8 / long_session: the batch and long-session "
                          "configurations, reported without e2e")
     args = ap.parse_args()
+    if args.oracle_one_thread:   # child mode of oracle_one_thread_child (host only)
+        print(json.dumps(oracle_one_thread()), flush=True)
+        return
     if args.warmup < 3:
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
 
@@ -885,7 +927,8 @@ def main():
         line["cpu_baseline"] = {"value": round(n / dt, 1), "unit": UNIT, "cores": cpu_threads(sh.n_v_heads),
                                 "kind": "oracle", "cpu": cpu_model(),
                                 "sample": f"first {n} tokens of the {w.session_lengths[0]}-token session, all "
-                                          f"{sh.n_v_heads} heads, one fp64 oracle call ({dt:.1f} s)"}
+                                          f"{sh.n_v_heads} heads, one fp64 oracle call ({dt:.1f} s)",
+                                "one_thread": oracle_one_thread_child()}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
