@@ -353,9 +353,13 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         *reinterpret_cast<uint4 *>(lo + off) = l;
     };
 
-    // beta v of the staged v-head (row-parallel conv, 4 rows per warp) into channels 128..255 of the B operand
-    auto conv_v = [&]() {
-        conv_rows(rawv, wv, 4 * warp, 4, [&](int i0, float (&y)[4][4]) {
+    // beta v of the staged v-head (row-parallel conv, groups of 4 rows) into channels 128..255 of the B operand:
+    // every warp takes the 4-row group `warp` (all), or, while thread 0 issues the Q K^T product, warps 1-15
+    // take the 16 groups, warp 1 two of them (without_warp0)
+    auto conv_v = [&](bool without_warp0) {
+        if (without_warp0 && warp == 0) return;
+        const int g0 = without_warp0 ? warp - 1 : warp, ng = without_warp0 && warp == 1 ? 2 : 1;
+        auto emit = [&](int i0, float (&y)[4][4]) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int i = i0 + u;
@@ -364,7 +368,24 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
                 for (int c = 0; c < 4; ++c) v[c] = i < n ? bet[i] * y[u][c] : 0.f;
                 split4_store(Bh, Bl, mnmajor_bf16_offset(128 + 4 * lane, i, B_LBO, B_SBO), v);
             }
-        });
+        };
+#pragma unroll 1
+        for (int k = 0; k < ng; ++k) conv_rows(rawv, wv, 4 * (k == 0 ? g0 : 15), 4, emit);   // group 15 to warp 1
+    };
+    // channels 0..127 of the B operand: beta e^gamma k_hat (from the hi/lo rows), 1024 groups of 8 channels,
+    // over threads first .. 511
+    auto b_khat = [&](int first) {
+        for (int e = t - first; e < 64 * 16; e += kUmmaPrepThreads - first) {
+            if (e < 0) break;
+            const int j = e & 63, cg = e >> 6;
+            const uint32_t o = kmajor_bf16_offset(64 + j, 8 * cg, AQ_LBO, AQ_SBO);
+            float v[8];
+            join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), v);
+            const float sc = bet[j] * egv[j];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v[c] *= sc;
+            store8(Bh, Bl, mnmajor_bf16_offset(8 * cg, j, B_LBO, B_SBO), v);
+        }
     };
 
     stage(cur, hk * p.G, true, p.debug_skip_first_copy == 2);   // 1. the first task's tiles
@@ -432,11 +453,11 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
                 split4_store(AQh, AQl, kmajor_bf16_offset(64 * which + i, 4 * lane, AQ_LBO, AQ_SBO), v);
             }
         });
-        conv_v();   // the first v-head's beta v in the same phase
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        // 3. [Q K^T; K K^T] = [q_hat; k_hat] k_hat^T into TMEM columns 0..63
+        // 3. [Q K^T; K K^T] = [q_hat; k_hat] k_hat^T into TMEM columns 0..63 (the first v-head's B operand is
+        //    built on warps 1-15 meanwhile)
         if (t == 0)
             mma3(tmem, umma_smem_desc(AQh, AQ_LBO, AQ_SBO), umma_smem_desc(AQl, AQ_LBO, AQ_SBO), 2 * AQ_LBO,
                  umma_smem_desc(AQh + 8 * AQ_SBO, AQ_LBO, AQ_SBO), umma_smem_desc(AQl + 8 * AQ_SBO, AQ_LBO, AQ_SBO),
@@ -475,20 +496,10 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             if (part == 0 && t == 32) rec[320 * D] = expf(gl);
         };
 
-        // 5. B operand, MN-major: channels 128..255 = beta v (the first v-head's came with the q/k conv),
-        //    channels 0..127 = beta e^gamma k_hat (from the hi/lo rows)
-        if (gi > 0) conv_v();
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int j = t & 63, cg = (t >> 6) + 8 * it;
-            const uint32_t o = kmajor_bf16_offset(64 + j, 8 * cg, AQ_LBO, AQ_SBO);
-            float v[8];
-            join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), v);
-            const float sc = bet[j] * egv[j];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) v[c] *= sc;
-            store8(Bh, Bl, mnmajor_bf16_offset(8 * cg, j, B_LBO, B_SBO), v);
-        }
+        // 5. B operand, MN-major: channels 128..255 = beta v, channels 0..127 = beta e^gamma k_hat; for the
+        //    first v-head on warps 1-15 while thread 0 issues the Q K^T product
+        conv_v(gi == 0);
+        b_khat(gi == 0 ? 32 : 0);
         fence_proxy_async();
         if (gi == 0) {
             if (!(ok = wait_mma())) break;   // Q K^T / K K^T landed in TMEM
