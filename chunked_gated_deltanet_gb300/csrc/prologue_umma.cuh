@@ -422,7 +422,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         egv[jg] = expf(sv);
     };
     gates_store(gates_load(cur, hk * p.G));
-    Gv gnext{0.f, 0.f, 0.f};
+    Gv gnext{0.f, 0.f, 0.f}, ghead{0.f, 0.f, 0.f};
     bool ok = true;
     for (;;) {   // tasks
     ok = wait_in();
@@ -468,9 +468,8 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     // 4. each v-head of the group
     for (int gi = 0; ok && gi < p.G; ++gi) {
         const int h = hk * p.G + gi;
-        if (gi > 0) {   // the previous head is done with the raw-tile region and every MMA operand
-            stage(cur, h, false, false);
-            gates_store(gates_load(cur, h));
+        if (gi > 0) {   // this head's v tile was staged during the previous head's record epilogue
+            gates_store(ghead);
             if (!(ok = wait_in())) break;
         }
         float *rec = p.ws_wu + ((int64_t)blk * Hv + h) * rec_floats(D);
@@ -651,8 +650,12 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         kt_record(1);
         if (!(ok = wait_mma())) break;
 
-        // the next task's inputs: the raw-tile region and the weights are free from here on
-        if (gi == p.G - 1 && (ntau = src.next()) >= 0) {
+        // the next v-head's v tile, or the next task's inputs: the raw-tile region and the weights are free
+        // from here on (the gates go to shared memory once this head's record is written)
+        if (gi + 1 < p.G) {
+            stage(cur, h + 1, false, false);
+            ghead = gates_load(cur, h + 1);
+        } else if ((ntau = src.next()) >= 0) {
             nxt = task_of(ntau);
             stage(nxt, nxt.hk * p.G, true, false);
             gnext = gates_load(nxt, nxt.hk * p.G);
