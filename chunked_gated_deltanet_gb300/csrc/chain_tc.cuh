@@ -11,8 +11,7 @@
 // prologue, or here for U'), accumulation is fp32. The prologue stores each
 // block's operands in fragment order, so a block is a few contiguous bulk
 // copies (TMA) issued by one thread into a two-stage buffer and completed on
-// an mbarrier. The compute runs on warps 0-7 (the first kThreads threads of
-// the CTA); a CTA may have more warps, which take no part in it.
+// an mbarrier. The compute runs on the CTA's 8 warps (kThreads threads).
 #pragma once
 #include "common.cuh"
 #include "mma.cuh"
@@ -38,7 +37,7 @@ struct ChainPlan {
     }
 };
 
-// Barrier of the chain's compute warps (0-7) alone.
+// Barrier of the chain's compute warps (all of the CTA's 8 warps).
 __device__ __forceinline__ void chain_bar() { asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads) : "memory"); }
 
 template <int D, int DS>
