@@ -115,6 +115,26 @@ def test_decode_steps_match_oracle(cuda_device):
     _check(run, sess, out, 517, o_ref, ST_ref, cs_ref)
 
 
+@pytest.mark.parametrize("dtype,d,act,q_scale", [(wl.FP32, 64, gdn.GDN_CONV_NONE, 1.0),
+                                                  (wl.BF16, 128, gdn.GDN_CONV_SILU, 128 ** -0.5),
+                                                  (wl.BF16, 64, gdn.GDN_CONV_NONE, 1.0)],
+                         ids=["fp32_d64", "bf16_d128_silu_qscale", "bf16_d64"])
+def test_decode_variants_match_oracle(cuda_device, dtype, d, act, q_scale):
+    """Decode steps after a prefill, for fp32 inputs, the SiLU conv with a q scale, and d = 64 (GQA layer,
+    two v-heads per q/k head): outputs, state and conv state against the oracle."""
+    shape = wl.Shape(2, 4, d, d, 64, dtype)
+    w = wl.Workload("decv", shape, seed=17, session_lengths=[132])
+    tok, cw = w.session_tokens(0), w.conv_weights()
+    run = Runner(shape, tok, cw, cuda_device, act=act, q_scale=q_scale)
+    sess, out = run.session(), run.new_out()
+    assert run.prefill(sess, 0, 132, out) == 128
+    for t in range(128, 132):
+        gdn.gdn_decode_step(run.desc, [sess], *(x[t:t + 1] for x in run.x), run.cw_t, out[t:t + 1])
+    assert sess.committed == 132
+    o_ref, ST_ref, cs_ref = oracle_run(shape, tok, cw, act=act, q_scale=q_scale)
+    _check(run, sess, out, 132, o_ref, ST_ref, cs_ref)
+
+
 def test_decode_batch_equals_single(cuda_device):
     """A decode step over 3 sessions equals three single-session steps, bit for bit."""
     shape = wl.Shape(2, 4, 64, 64, 64, wl.BF16)
