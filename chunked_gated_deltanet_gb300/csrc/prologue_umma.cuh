@@ -136,11 +136,15 @@ __device__ __forceinline__ void put_cfrag16(float *base, int i, int c0, const fl
     }
 }
 
-// c += X Y for a 16 x K block of X (row-major, pitch lx) and a K x 8 block of Y (row-major, pitch ly),
-// m16n8k8 tf32 MMAs with split operands (hi*hi + hi*lo + lo*hi: close to fp32 products); one warp.
-__device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, int lx, const float *Y, int ly, int K,
-                                               int lane) {
+// c = X Y for a 16 x K block of X (row-major, pitch lx) and a K x 8 block of Y (row-major, pitch ly),
+// m16n8k8 tf32 MMAs with split operands (hi*hi + hi*lo + lo*hi: close to fp32 products); one warp. The
+// three partial products accumulate apart, so the dependent chain is K / 8 MMAs long, and the two small
+// ones are added together before they join the large one.
+template <int K>
+__device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, int lx, const float *Y, int ly, int lane) {
     const int g = lane >> 2, t = lane & 3;
+    float hh[4] = {0.f, 0.f, 0.f, 0.f}, hl[4] = {0.f, 0.f, 0.f, 0.f}, lh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
     for (int k0 = 0; k0 < K; k0 += 8) {
         uint32_t ah[4], al[4], bh[2], bl[2];
         split_tf32(X[g * lx + k0 + t], ah[0], al[0]);
@@ -149,11 +153,17 @@ __device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, in
         split_tf32(X[(g + 8) * lx + k0 + t + 4], ah[3], al[3]);
         split_tf32(Y[(k0 + t) * ly + g], bh[0], bl[0]);
         split_tf32(Y[(k0 + t + 4) * ly + g], bh[1], bl[1]);
-        mma_tf32(c, al, bh);
-        mma_tf32(c, ah, bl);
-        mma_tf32(c, ah, bh);
+        mma_tf32(lh, al, bh);
+        mma_tf32(hl, ah, bl);
+        mma_tf32(hh, ah, bh);
     }
+#pragma unroll
+    for (int f = 0; f < 4; ++f) c[f] = hh[f] + (hl[f] + lh[f]);
 }
+// named barrier `id` over n threads (whole warps): bar_sync waits, bar_arrive only signals (its earlier
+// shared-memory writes are visible to the threads that wait on the same barrier)
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void bar_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 // the m16n8 C fragment c (times s) into a row-major block Z (pitch lz)
 __device__ __forceinline__ void store_c16x8(float *Z, int lz, const float (&c)[4], float s, int lane) {
     const int g = lane >> 2, t = lane & 3;
@@ -541,12 +551,16 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         tc_fence_before();
         __syncthreads();
 
-        // 7. T = (I + A)^{-1} (unit lower triangular) in fp32, two levels of 2x2 blocking:
-        //    diagonal 16x16 blocks D_b by substitution (one column per thread, warp 0: D_0, D_1, warp 1: D_2,
-        //    D_3; the other threads zero the blocks above the diagonal), then on the same warps
-        //    T_10 = -D_1 A_10 D_0 and T_32 = -D_3 A_32 D_2, then T[32:64, 0:32] = -T[32:64, 32:64] A[32:64, 0:32]
-        //    T[0:32, 0:32] on warps 0-3, one 8-column tile each; products as split-tf32 MMAs. A warp reads only
-        //    what it wrote between the CTA barriers, so warp barriers order the steps within a level.
+        // 7. T = (I + A)^{-1} (unit lower triangular) in fp32, two levels of 2x2 blocking, products as
+        //    split-tf32 MMAs, one 16 x 8 tile per warp:
+        //    (a) diagonal 16x16 blocks D_b by substitution, one column per thread (warp 0: D_0, D_1; warp 1:
+        //        D_2, D_3); warps 8-15 zero the blocks above the diagonal meanwhile;
+        //    (b) warps 0-3 (block pair (b + 1, b), column tile nt): T_10 = -D_1 (A_10 D_0), T_32 = -D_3 (A_32 D_2);
+        //    (c) warps 0-7 (row tile mt, column tile nt): X = A[32:64, 0:32] T[0:32, 0:32], then
+        //        T[32:64, 0:32] = -T[32:64, 32:64] X.
+        //    Products skip the zero blocks of T, whose writes need only be done by the CTA barrier after (c).
+        //    Named barriers order the levels: 1 (warps 0-3), 2 (warps 0-7), 3 + nt (X tile (0, nt) from warp
+        //    nt to warp 4 + nt).
         constexpr int LM = 24, LX = 40;
         float *Xs = reinterpret_cast<float *>(TBh);   // 32 x LX scratch (the T operand regions are written later)
         if (t < kBlock) {
@@ -563,45 +577,42 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tf[(16 * d + i) * LT + 16 * d + c] = x[i];
-            __syncwarp();
-            const int b = 2 * warp;   // block pair (b + 1, b)
-            float *M = Mt + warp * 16 * LM;
-#pragma unroll 1
-            for (int nt = 0; nt < 2; ++nt) {
-                float cc[4] = {0.f, 0.f, 0.f, 0.f};
-                mma3_tf32_16x8(cc, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, 16, lane);
-                store_c16x8(M + 8 * nt, LM, cc, 1.f, lane);
-            }
-            __syncwarp();
-#pragma unroll 1
-            for (int nt = 0; nt < 2; ++nt) {
-                float cc[4] = {0.f, 0.f, 0.f, 0.f};
-                mma3_tf32_16x8(cc, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, M + 8 * nt, LM, 16, lane);
-                store_c16x8(Tf + 16 * (b + 1) * LT + 16 * b + 8 * nt, LT, cc, -1.f, lane);
-            }
-        } else {
-            for (int e = t - kBlock; e < 6 * 64; e += kUmmaPrepThreads - kBlock) {   // 6 blocks x 16 rows x 4 float4
+        } else if (t >= 256) {
+            for (int e = t - 256; e < 6 * 64; e += kUmmaPrepThreads - 256) {   // 6 blocks x 16 rows x 4 float4
                 const int bi = e >> 6, r = (e >> 2) & 15, c4 = e & 3;
                 const int ib = bi < 3 ? 0 : (bi < 5 ? 1 : 2), jb = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
                 *reinterpret_cast<float4 *>(Tf + (16 * ib + r) * LT + 16 * jb + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        __syncthreads();
-        if (warp < 4) {   // column tile nt = warp: X = A[32:64, 0:32] T[0:32, 0:32], then T[32:64, 0:32] = -T[32:64, 32:64] X
-            const int nt = warp;
-#pragma unroll 1
-            for (int mt = 0; mt < 2; ++mt) {
-                float cc[4] = {0.f, 0.f, 0.f, 0.f};
-                mma3_tf32_16x8(cc, Af + (32 + 16 * mt) * LT, LT, Tf + 8 * nt, LT, 32, lane);
-                store_c16x8(Xs + 16 * mt * LX + 8 * nt, LX, cc, 1.f, lane);
-            }
+        if (warp < 4) {   // (b)
+            bar_sync(1, 128);
+            const int b = 2 * (warp >> 1), nt = warp & 1;
+            float *M = Mt + (warp >> 1) * 16 * LM;
+            float cc[4];
+            mma3_tf32_16x8<16>(cc, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, lane);
+            store_c16x8(M + 8 * nt, LM, cc, 1.f, lane);
             __syncwarp();
-#pragma unroll 1
-            for (int mt = 0; mt < 2; ++mt) {
-                float cc[4] = {0.f, 0.f, 0.f, 0.f};
-                mma3_tf32_16x8(cc, Tf + (32 + 16 * mt) * LT + 32, LT, Xs + 8 * nt, LX, 32, lane);
-                store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, cc, -1.f, lane);
+            mma3_tf32_16x8<16>(cc, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, M + 8 * nt, LM, lane);
+            store_c16x8(Tf + 16 * (b + 1) * LT + 16 * b + 8 * nt, LT, cc, -1.f, lane);
+        }
+        if (warp < 8) {   // (c)
+            bar_sync(2, 256);
+            const int nt = warp & 3, mt = warp >> 2;
+            float cc[4];
+            // T[0:16, 16:32] = 0: column tiles 2 and 3 of T[0:32, 0:32] need only its rows 16..31
+            if (nt < 2) mma3_tf32_16x8<32>(cc, Af + (32 + 16 * mt) * LT, LT, Tf + 8 * nt, LT, lane);
+            else mma3_tf32_16x8<16>(cc, Af + (32 + 16 * mt) * LT + 16, LT, Tf + 16 * LT + 8 * nt, LT, lane);
+            store_c16x8(Xs + 16 * mt * LX + 8 * nt, LX, cc, 1.f, lane);
+            // T[32:48, 48:64] = 0: row tile 0 needs only X rows 0..15 (its own tile), row tile 1 all 32
+            if (mt == 0) {
+                bar_arrive(3 + nt, 64);
+                __syncwarp();
+                mma3_tf32_16x8<16>(cc, Tf + 32 * LT + 32, LT, Xs + 8 * nt, LX, lane);
+            } else {
+                bar_sync(3 + nt, 64);
+                mma3_tf32_16x8<32>(cc, Tf + 48 * LT + 32, LT, Xs + 8 * nt, LX, lane);
             }
+            store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, cc, -1.f, lane);
         }
         __syncthreads();
         //    T as bf16 hi/lo: rows 0..63 of [T; P T] (K-major, written over A and T) and the B operand of
