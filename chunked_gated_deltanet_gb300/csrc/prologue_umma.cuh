@@ -78,12 +78,13 @@ struct UmmaCtl {
 
 // A persistent CTA's tasks: blockIdx.x, + gridDim.x, ... of the launch's nblk x Hk tasks, task tau =
 // (block tau % nblk, q/k head tau / nblk). A task source hands out task indices in the order the CTA runs
-// them (first(), then next() until it returns -1, all CTA-uniform) and is told when a task's record is
-// complete (done()).
+// them (first(), then next() until it returns -1, all CTA-uniform), tells which task next() will return
+// (peek(), -1 if none) and is told when a task's record is complete (done()).
 struct StridedTasks {
     int tau, ntask;
     __device__ __forceinline__ int first() { return tau < ntask ? tau : -1; }
     __device__ __forceinline__ int next() { tau += gridDim.x; return tau < ntask ? tau : -1; }
+    __device__ __forceinline__ int peek() const { return tau + (int)gridDim.x < ntask ? tau + (int)gridDim.x : -1; }
     __device__ __forceinline__ void done(int, int) {}
 };
 
@@ -383,10 +384,14 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         for (int k = 0; k < ng; ++k) conv_rows(rawv, wv, 4 * (k == 0 ? g0 : 15), 4, emit);   // group 15 to warp 1
     };
     // channels 0..127 of the B operand: beta e^gamma k_hat (from the hi/lo rows), 1024 groups of 8 channels,
-    // over threads first .. 511
-    auto b_khat = [&](int first) {
-        for (int e = t - first; e < 64 * 16; e += kUmmaPrepThreads - first) {
-            if (e < 0) break;
+    // over every thread, or (for the first v-head, where warp 1 takes two conv groups and warp 0 joins after
+    // issuing the Q K^T product) over every thread but warp 1's
+    auto b_khat = [&](bool without_warp1) {
+        if (without_warp1 && warp == 1) return;
+        // (warp 0 ranks last there, so that the 64 threads with a third group are in warps 2 and 3)
+        const int r0 = !without_warp1 ? t : (warp == 0 ? kUmmaPrepThreads - 64 + lane : t - 64);
+        const int nr = without_warp1 ? kUmmaPrepThreads - 32 : kUmmaPrepThreads;
+        for (int e = r0; e < 64 * 16; e += nr) {
             const int j = e & 63, cg = e >> 6;
             const uint32_t o = kmajor_bf16_offset(64 + j, 8 * cg, AQ_LBO, AQ_SBO);
             float v[8];
@@ -436,6 +441,15 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     bool ok = true;
     for (;;) {   // tasks
     ok = wait_in();
+    if (ok && t == 32) {   // the next task's input tiles into L2, a task ahead of the copies that stage them
+        const int pt = src.peek();
+        if (pt >= 0) {
+            const Task k = task_of(pt);
+            tma_prefetch_2d(&p.tm_q, k.hk * D, (int)k.row0);
+            tma_prefetch_2d(&p.tm_k, k.hk * D, (int)k.row0);
+            for (int gi = 0; gi < p.G; ++gi) tma_prefetch_2d(&p.tm_v, (k.hk * p.G + gi) * D, (int)k.row0);
+        }
+    }
 
     if (ok) {
         // 2. conv + L2 norm of q (warps 0-7) and k (warps 8-15), 8 rows per warp -> bf16 hi/lo rows of [q_hat; k_hat]
@@ -508,7 +522,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         // 5. B operand, MN-major: channels 128..255 = beta v, channels 0..127 = beta e^gamma k_hat; for the
         //    first v-head on warps 1-15 while thread 0 issues the Q K^T product
         conv_v(gi == 0);
-        b_khat(gi == 0 ? 32 : 0);
+        b_khat(gi == 0);
         fence_proxy_async();
         if (gi == 0) {
             if (!(ok = wait_mma())) break;   // Q K^T / K K^T landed in TMEM
@@ -671,19 +685,20 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             stage(nxt, nxt.hk * p.G, true, false);
             gnext = gates_load(nxt, nxt.hk * p.G);
         }
-        // 11. the record, every warp (lanes 32 (warp % 4) .., 64 columns at 64 (warp / 4)):
+        // 11. the record, every warp (lanes 32 (warp % 4) .., the 16-column chunks warp / 4 + 4 j, j = 0..3: two of
+        //     [W; P W] and two of [U; P U], so that every warp has the same share of the costlier first kind):
         //     W rows -> tf32 A fragments (rows 0..63 of [W; Qe]); U rows -> C fragments;
         //     P W rows -> Qe = e^gamma q_hat - P W (rows 64..127 of [W; Qe]); P U rows -> O_intra C fragments
         {
             const int R = 32 * (warp & 3) + lane, cp = warp >> 2;
             const bool top = R < kBlock;
             const int i = top ? R : R - kBlock;
-            const uint32_t tb = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 + 64 * cp;
+            const uint32_t tb = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
-                const int c0 = 64 * cp + 16 * cc;
+                const int c0 = 16 * (cp + 4 * cc);
                 float v[16];
-                tmem_ld16(tb + 16 * cc, v);
+                tmem_ld16(tb + c0, v);
                 if (c0 < D) {
                     if (top) {
 #pragma unroll
