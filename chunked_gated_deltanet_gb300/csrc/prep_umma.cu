@@ -8,6 +8,16 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     prep_umma_kernel(const __grid_constant__ LaunchCommon p, int64_t ch) {
     extern __shared__ __align__(1024) unsigned char sm[];
     UmmaCtl *ctl = reinterpret_cast<UmmaCtl *>(sm + up::OFF_BAR);
+    if (threadIdx.x == 32 && (int)blockIdx.x < p.nblk * p.Hk) {
+        // The first task's input tiles into L2 while this CTA waits for earlier work. A prefetch only
+        // places lines in L2, the point of coherence, so a write that lands later still wins.
+        const int blk = (int)blockIdx.x % p.nblk, hk = (int)blockIdx.x / p.nblk;
+        const SessRef s = p.s[find_session(p, blk)];
+        const int row0 = (int)(s.row0 + (int64_t)(blk - s.blk0) * kBlock);
+        tma_prefetch_2d(&p.tm_q, hk * up::D, row0);
+        tma_prefetch_2d(&p.tm_k, hk * up::D, row0);
+        for (int gi = 0; gi < p.G; ++gi) tma_prefetch_2d(&p.tm_v, (hk * p.G + gi) * up::D, row0);
+    }
     if ((threadIdx.x >> 5) == 0) {
         tmem_alloc(&ctl->tslot, 512);
         tmem_relinquish();
