@@ -4,6 +4,9 @@
 
 namespace gdn {
 
+// kAct: SiLU after the causal conv (LaunchCommon::act), as a template parameter so that the instantiation
+// without it keeps its loop compact.
+template <bool kAct>
 __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     prep_umma_kernel(const __grid_constant__ LaunchCommon p, int64_t ch) {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -29,7 +32,7 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     grid_dep_launch();   // the state kernel may take SMs as this kernel's CTAs leave
     grid_dep_wait();     // inputs and conv state of this call, written by earlier work
     StridedTasks src{(int)blockIdx.x, p.nblk * p.Hk};
-    prologue_run(p, ch, sm, ctl, tmem, src);
+    prologue_run<kAct>(p, ch, sm, ctl, tmem, src);
     tc_fence_after();
     if ((threadIdx.x >> 5) == 0) tmem_dealloc(tmem, 512);
 }
@@ -38,11 +41,12 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
 
 cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st) {
     using namespace gdn;
-    cudaError_t e = cudaFuncSetAttribute(prep_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)up::SMEM);
+    auto k = p.act ? prep_umma_kernel<true> : prep_umma_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)up::SMEM);
     if (e != cudaSuccess) return e;
     int sms = 1;   // one persistent CTA per SM (shared memory allows no more), over nblk x Hk tasks
     if ((e = gdn_sm_count(&sms)) != cudaSuccess) return e;
     const int ntask = p.nblk * p.Hk;
-    e = gdn_launch_pdl(prep_umma_kernel, ntask < sms ? ntask : sms, kUmmaPrepThreads, up::SMEM, st, p, ch);
+    e = gdn_launch_pdl(k, ntask < sms ? ntask : sms, kUmmaPrepThreads, up::SMEM, st, p, ch);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -137,15 +137,16 @@ __device__ __forceinline__ void put_cfrag16(float *base, int i, int c0, const fl
     }
 }
 
-// c = X Y for a 16 x K block of X (row-major, pitch lx) and a K x 8 block of Y (row-major, pitch ly),
-// m16n8k8 tf32 MMAs with split operands (hi*hi + hi*lo + lo*hi: close to fp32 products); one warp. The
-// three partial products accumulate apart, so the dependent chain is K / 8 MMAs long, and the two small
-// ones are added together before they join the large one.
-template <int K>
-__device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, int lx, const float *Y, int ly, int lane) {
+// c = X Y for a 16 x K block of X (row-major, pitch lx) and a K x 8 block of Y (row-major, pitch ly), K a
+// multiple of 8, m16n8k8 tf32 MMAs with split operands (hi*hi + hi*lo + lo*hi: close to fp32 products); one
+// warp. The three partial products accumulate apart, so the dependent chain is K / 8 MMAs long, and the two
+// small ones are added together before they join the large one. The k loop stays rolled: its chain is
+// latency-bound either way, and the compact code keeps the caller's loop within the instruction caches.
+__device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, int lx, const float *Y, int ly, int K,
+                                               int lane) {
     const int g = lane >> 2, t = lane & 3;
     float hh[4] = {0.f, 0.f, 0.f, 0.f}, hl[4] = {0.f, 0.f, 0.f, 0.f}, lh[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
     for (int k0 = 0; k0 < K; k0 += 8) {
         uint32_t ah[4], al[4], bh[2], bl[2];
         split_tf32(X[g * lx + k0 + t], ah[0], al[0]);
@@ -197,7 +198,7 @@ __device__ __forceinline__ void join8(uint4 hi, uint4 lo, float *v) {
 // during the current task's record epilogue. Returns false if a bounded wait ran out (the error word is
 // set, nothing is left in flight). The mbarriers are initialised on entry and invalidated on return, so
 // the plan's memory may serve other uses between calls.
-template <class Src>
+template <bool kAct, class Src>
 __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, unsigned char *sm, UmmaCtl *ctl,
                                              uint32_t tmem, Src &src) {
     using namespace up;
@@ -341,7 +342,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
                     y[u][c] = conv_tap<__nv_bfloat16>(w[c], x[u][c], x[u + 1][c], x[u + 2][c], x[u + 3][c], 0);
-            if (p.act) {   // SiLU, as one branch after the taps so that the default path stays compact
+            if constexpr (kAct) {   // SiLU (a separate kernel instantiation, so the default one carries no code for it)
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
 #pragma unroll
@@ -603,10 +604,10 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             const int b = 2 * (warp >> 1), nt = warp & 1;
             float *M = Mt + (warp >> 1) * 16 * LM;
             float cc[4];
-            mma3_tf32_16x8<16>(cc, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, lane);
+            mma3_tf32_16x8(cc, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, 16, lane);
             store_c16x8(M + 8 * nt, LM, cc, 1.f, lane);
             __syncwarp();
-            mma3_tf32_16x8<16>(cc, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, M + 8 * nt, LM, lane);
+            mma3_tf32_16x8(cc, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, M + 8 * nt, LM, 16, lane);
             store_c16x8(Tf + 16 * (b + 1) * LT + 16 * b + 8 * nt, LT, cc, -1.f, lane);
         }
         if (warp < 8) {   // (c)
@@ -614,18 +615,17 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             const int nt = warp & 3, mt = warp >> 2;
             float cc[4];
             // T[0:16, 16:32] = 0: column tiles 2 and 3 of T[0:32, 0:32] need only its rows 16..31
-            if (nt < 2) mma3_tf32_16x8<32>(cc, Af + (32 + 16 * mt) * LT, LT, Tf + 8 * nt, LT, lane);
-            else mma3_tf32_16x8<16>(cc, Af + (32 + 16 * mt) * LT + 16, LT, Tf + 16 * LT + 8 * nt, LT, lane);
+            const int k0 = nt < 2 ? 0 : 16;
+            mma3_tf32_16x8(cc, Af + (32 + 16 * mt) * LT + k0, LT, Tf + k0 * LT + 8 * nt, LT, 32 - k0, lane);
             store_c16x8(Xs + 16 * mt * LX + 8 * nt, LX, cc, 1.f, lane);
             // T[32:48, 48:64] = 0: row tile 0 needs only X rows 0..15 (its own tile), row tile 1 all 32
             if (mt == 0) {
                 bar_arrive(3 + nt, 64);
                 __syncwarp();
-                mma3_tf32_16x8<16>(cc, Tf + 32 * LT + 32, LT, Xs + 8 * nt, LX, lane);
             } else {
                 bar_sync(3 + nt, 64);
-                mma3_tf32_16x8<32>(cc, Tf + 48 * LT + 32, LT, Xs + 8 * nt, LX, lane);
             }
+            mma3_tf32_16x8(cc, Tf + (32 + 16 * mt) * LT + 32, LT, Xs + 8 * nt, LX, 16 + 16 * mt, lane);
             store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, cc, -1.f, lane);
         }
         __syncthreads();
