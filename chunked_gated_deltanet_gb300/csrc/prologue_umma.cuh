@@ -88,6 +88,27 @@ struct StridedTasks {
     __device__ __forceinline__ void done(int, int) {}
 };
 
+// Packed fp32 pairs (sm_100 and later): each lane rounds as the scalar instruction does, so a pair of
+// scalar mul / fma chains and its packed form give the same bits.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &a, float &b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r)); }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// the two bf16 values of a 32-bit word as an fp32 pair (low half first)
+__device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t u) { return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u)); }
+
 // dst[0] = a, dst[1] = b in one 32-byte store (dst 32-byte aligned)
 __device__ __forceinline__ void st_v8(float4 *dst, float4 a, float4 b) {
     asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"l"(dst), "f"(a.x), "f"(a.y), "f"(a.z), "f"(a.w),
@@ -314,34 +335,44 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     };
 
     // Row-parallel conv of rows [r0, r0 + nr) of a staged tile: lane owns channels 4 lane .. 4 lane + 3,
-    // four rows at a time; outputs go through emit(i0, y[4][4]).
+    // four rows at a time; outputs go through emit(i0, y[4][4]). The taps run on channel pairs in packed
+    // fp32 (oldest tap first: a product, then three fmas, per channel).
     auto conv_rows = [&](const __nv_bfloat16 *raw, const __nv_bfloat16 *wsm, int r0, int nr, auto &&emit) {
-        float w[4][4];
+        uint64_t w2[2][4];   // [channel pair][tap]
         {
             const uint4 u0 = *reinterpret_cast<const uint4 *>(wsm + lane * 16);
             const uint4 u1 = *reinterpret_cast<const uint4 *>(wsm + lane * 16 + 8);
-            const uint32_t ww[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            const uint32_t ww[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};   // channel c: ww[2c], ww[2c + 1]
+            float w[4][4];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 w[e >> 1][2 * (e & 1)] = __uint_as_float(ww[e] << 16);
                 w[e >> 1][2 * (e & 1) + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
             }
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) w2[q][k] = f2_pack(w[2 * q][k], w[2 * q + 1][k]);
         }
         for (int i0 = r0; i0 < r0 + nr; i0 += 4) {
-            float x[7][4];   // raw rows i0 .. i0+6 = block rows i0-3 .. i0+3
+            uint64_t x2[7][2];   // raw rows i0 .. i0+6 = block rows i0-3 .. i0+3, channel pairs
 #pragma unroll
             for (int r = 0; r < 7; ++r) {
                 const uint2 u = *reinterpret_cast<const uint2 *>(raw + (i0 + r) * D + lane * 4);
-                const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-                const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-                x[r][0] = __low2float(a); x[r][1] = __high2float(a); x[r][2] = __low2float(b); x[r][3] = __high2float(b);
+                x2[r][0] = f2_from_bf16x2(u.x);
+                x2[r][1] = f2_from_bf16x2(u.y);
             }
             float y[4][4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    y[u][c] = conv_tap<__nv_bfloat16>(w[c], x[u][c], x[u + 1][c], x[u + 2][c], x[u + 3][c], 0);
+                for (int q = 0; q < 2; ++q) {
+                    uint64_t a = f2_mul(w2[q][0], x2[u][q]);
+                    a = f2_fma(w2[q][1], x2[u + 1][q], a);
+                    a = f2_fma(w2[q][2], x2[u + 2][q], a);
+                    a = f2_fma(w2[q][3], x2[u + 3][q], a);
+                    f2_unpack(a, y[u][2 * q], y[u][2 * q + 1]);
+                }
             if constexpr (kAct) {   // SiLU (a separate kernel instantiation, so the default one carries no code for it)
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
