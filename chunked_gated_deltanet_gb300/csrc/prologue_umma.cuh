@@ -321,10 +321,13 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         tc_fence_after();
         return true;
     };
-    // bf16 hi/lo MMA group D (+)= A B over K (3 passes per 16-wide K-step), then a commit; thread 0 only
+    // bf16 hi/lo MMA group D (+)= A B over K (3 passes per 16-wide K-step), then a commit; thread 0 only.
+    // The loop stays rolled (the issue is serial either way; compact code keeps the task loop in the
+    // instruction caches).
     auto mma3 = [&](uint32_t d, uint64_t ah, uint64_t al, uint32_t astep, uint64_t bh, uint64_t bl, uint32_t bstep,
                     int K, uint32_t id) {
         tc_fence_after();
+#pragma unroll 1
         for (int ks = 0; ks < K / 16; ++ks) {
             const uint64_t oa = (astep * ks) >> 4, ob = (bstep * ks) >> 4;
             umma_bf16(d, ah + oa, bh + ob, id, ks > 0);
@@ -708,13 +711,18 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
 
         // the next v-head's v tile, or the next task's inputs: the raw-tile region and the weights are free
         // from here on (the gates go to shared memory once this head's record is written)
-        if (gi + 1 < p.G) {
-            stage(cur, h + 1, false, false);
-            ghead = gates_load(cur, h + 1);
-        } else if ((ntau = src.next()) >= 0) {
-            nxt = task_of(ntau);
-            stage(nxt, nxt.hk * p.G, true, false);
-            gnext = gates_load(nxt, nxt.hk * p.G);
+        // (one call site for both, so that the staging code appears once)
+        {
+            const bool next_head = gi + 1 < p.G;
+            if (!next_head && (ntau = src.next()) >= 0) nxt = task_of(ntau);
+            if (next_head || ntau >= 0) {
+                const Task k = next_head ? cur : nxt;
+                const int hs = next_head ? h + 1 : nxt.hk * p.G;
+                stage(k, hs, !next_head, false);
+                const Gv gv = gates_load(k, hs);
+                if (next_head) ghead = gv;
+                else gnext = gv;
+            }
         }
         // 11. the record, every warp (lanes 32 (warp % 4) .., the 16-column chunks warp / 4 + 4 j, j = 0..3: two of
         //     [W; P W] and two of [U; P U], so that every warp has the same share of the costlier first kind):
