@@ -23,11 +23,14 @@
 // Operands live in shared memory in the no-swizzle layouts of umma.cuh: the
 // row-ordered operands (q_hat, k_hat, P, T, P T) K-major, the token-by-channel
 // B operands MN-major, so that every producer writes whole 16-byte
-// core-matrix rows. The triangular inverse stays in fp32 on the CUDA cores.
-// The input tiles arrive as 2-D tensor copies (one per tile) plus three
-// single-row halo copies, on an mbarrier; every wait is bounded, and on a
-// timeout the CTA records it in the device error word, waits (bounded) for
-// what it has in flight and returns (the kernel then frees its TMEM).
+// core-matrix rows. The triangular inverse stays in fp32: substitution on the
+// CUDA cores for its 16 x 16 diagonal blocks, split-tf32 mma.sync for the
+// blocked products. The input tiles arrive as 2-D tensor copies (one per tile)
+// plus three single-row halo copies, on an mbarrier: a task's tiles are
+// prefetched into L2 at the start of the task before it and copied in during
+// that task's record epilogue. Every wait is bounded, and on a timeout the CTA
+// records it in the device error word, waits (bounded) for what it has in
+// flight and returns (the kernel then frees its TMEM).
 #pragma once
 #include "common.cuh"
 #include "mma.cuh"
