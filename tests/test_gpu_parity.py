@@ -49,6 +49,8 @@ CASES = [
     (2, 4, 128, 128, 650, True, 0, 1.0, gdn.GDN_BF16),
     (3, 6, 64, 64, 1, True, 0, 1.0, gdn.GDN_FP32),
     (2, 2, 128, 64, 64, False, 0, 1.0, gdn.GDN_FP32),
+    (1, 4, 128, 64, 300, True, 0, 1.0, gdn.GDN_FP32),   # four v-heads per q/k head
+    (2, 4, 128, 64, 333, True, 1, 0.7, gdn.GDN_FP32),   # SiLU conv with two v-heads per q/k head
 ]
 
 
