@@ -161,6 +161,14 @@ __device__ __forceinline__ void put_cfrag16(float *base, int i, int c0, const fl
     }
 }
 
+// x = hi + lo exactly, hi the tf32 truncation of x (low 13 bits cleared), lo the rest in fp32. The MMA
+// reads lo as tf32 by dropping its low 13 bits, so a split product misses at most about 2^-20 |x| of each
+// operand: far below the bf16 hi/lo split (about 2^-16) that the inverse's result goes through next.
+__device__ __forceinline__ void split_tf32_trunc(float x, uint32_t &hi, uint32_t &lo) {
+    hi = __float_as_uint(x) & 0xFFFFE000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
 // c = X Y for a 16 x K block of X (row-major, pitch lx) and a K x 8 block of Y (row-major, pitch ly), K a
 // multiple of 8, m16n8k8 tf32 MMAs with split operands (hi*hi + hi*lo + lo*hi: close to fp32 products); one
 // warp. The three partial products accumulate apart, so the dependent chain is K / 8 MMAs long, and the two
@@ -173,12 +181,12 @@ __device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, in
 #pragma unroll 1
     for (int k0 = 0; k0 < K; k0 += 8) {
         uint32_t ah[4], al[4], bh[2], bl[2];
-        split_tf32(X[g * lx + k0 + t], ah[0], al[0]);
-        split_tf32(X[(g + 8) * lx + k0 + t], ah[1], al[1]);
-        split_tf32(X[g * lx + k0 + t + 4], ah[2], al[2]);
-        split_tf32(X[(g + 8) * lx + k0 + t + 4], ah[3], al[3]);
-        split_tf32(Y[(k0 + t) * ly + g], bh[0], bl[0]);
-        split_tf32(Y[(k0 + t + 4) * ly + g], bh[1], bl[1]);
+        split_tf32_trunc(X[g * lx + k0 + t], ah[0], al[0]);
+        split_tf32_trunc(X[(g + 8) * lx + k0 + t], ah[1], al[1]);
+        split_tf32_trunc(X[g * lx + k0 + t + 4], ah[2], al[2]);
+        split_tf32_trunc(X[(g + 8) * lx + k0 + t + 4], ah[3], al[3]);
+        split_tf32_trunc(Y[(k0 + t) * ly + g], bh[0], bl[0]);
+        split_tf32_trunc(Y[(k0 + t + 4) * ly + g], bh[1], bl[1]);
         mma_tf32(lh, al, bh);
         mma_tf32(hl, ah, bl);
         mma_tf32(hh, ah, bh);
