@@ -626,14 +626,17 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         if (t < kBlock) {
             const int d = t >> 4, c = t & 15;
             const float *Ad = Af + 16 * d * LT + 16 * d;
+            // right-looking: once x_j is final, every later row takes its term (x_j = 0 for j < c adds
+            // nothing), so the dependent chain is one fma per row
             float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float sum = 0.f;
+            for (int i = 0; i < 16; ++i) x[i] = 0.f;
 #pragma unroll
-                for (int j = 0; j < i; ++j)
-                    if (j >= c) sum = fmaf(Ad[i * LT + j], x[j], sum);
-                x[i] = i < c ? 0.f : (i == c ? 1.f : -sum);
+            for (int j = 0; j < 16; ++j) {
+                const float xj = j < c ? 0.f : (j == c ? 1.f : x[j]);
+                x[j] = xj;
+#pragma unroll
+                for (int i = j + 1; i < 16; ++i) x[i] = fmaf(-Ad[i * LT + j], xj, x[i]);
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tf[(16 * d + i) * LT + 16 * d + c] = x[i];
