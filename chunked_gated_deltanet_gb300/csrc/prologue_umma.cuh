@@ -194,6 +194,19 @@ __device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, in
 #pragma unroll
     for (int f = 0; f < 4; ++f) c[f] = hh[f] + (hl[f] + lh[f]);
 }
+// The gates (g and beta, [rows][Hv] fp32) of rows [row0, row0 + n) into L2: the whole 16-byte granules
+// inside those rows only, so that the prefetch stays within the rows the task reads.
+__device__ __forceinline__ void prefetch_gates(const LaunchCommon &p, int64_t row0, int n) {
+    const float *arr[2] = {p.g, p.beta};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(arr[q] + row0 * p.Hv);
+        const uintptr_t hi = reinterpret_cast<uintptr_t>(arr[q] + (row0 + n) * p.Hv);
+        const uintptr_t s0 = (lo + 15) & ~uintptr_t(15), s1 = hi & ~uintptr_t(15);
+        if (s1 > s0) bulk_prefetch_l2(reinterpret_cast<const void *>(s0), (uint32_t)(s1 - s0));
+    }
+}
+
 // named barrier `id` over n threads (whole warps): bar_sync waits, bar_arrive only signals (its earlier
 // shared-memory writes are visible to the threads that wait on the same barrier)
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
@@ -487,13 +500,14 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     bool ok = true;
     for (;;) {   // tasks
     ok = wait_in();
-    if (ok && t == 32) {   // the next task's input tiles into L2, a task ahead of the copies that stage them
+    if (ok && t == 32) {   // the next task's input tiles and gates into L2, a task ahead of their loads
         const int pt = src.peek();
         if (pt >= 0) {
             const Task k = task_of(pt);
             tma_prefetch_2d(&p.tm_q, k.hk * D, (int)k.row0);
             tma_prefetch_2d(&p.tm_k, k.hk * D, (int)k.row0);
             for (int gi = 0; gi < p.G; ++gi) tma_prefetch_2d(&p.tm_v, (k.hk * p.G + gi) * D, (int)k.row0);
+            prefetch_gates(p, k.row0, k.n);
         }
     }
 

@@ -60,6 +60,11 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, i
                  : "memory");
 }
 
+// Prefetch of [a, a + bytes) into L2 (a and bytes multiples of 16; no completion to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *a, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(a), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t *smem_result, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(smem_result)),
                  "r"(ncols)
