@@ -194,3 +194,30 @@ def test_conv_state_readback(cuda_device):
     torch.cuda.synchronize()
     expect = np.concatenate([tok.xq[125:128], tok.xk[125:128], tok.xv[125:128]], axis=1)
     assert np.array_equal(host.view(torch.int16).numpy().view(np.uint16), expect)
+
+
+@pytest.mark.parametrize("kind", ["strong_decay", "no_decay", "alternating"])
+def test_extreme_gates_match_oracle(cuda_device, kind):
+    """Gates at the edges of their range, where the block's triangular system is least benign: beta near 1
+    with a log-decay of -3 per token (decays across a block underflow to zero), with none (g = 0, every
+    block's A at full strength), or alternating between the two. 700 tokens (ragged last block), two v-heads
+    per q/k head, d = 128 on the tensor-core prologue."""
+    shape = wl.Shape(2, 4, 128, 128, 64, wl.BF16)
+    T = 700
+    w = wl.Workload("gates", shape, seed=31, session_lengths=[T])
+    tok, cw = w.session_tokens(0), w.conv_weights()
+    rng = np.random.default_rng(5)
+    beta = (0.99 - 0.01 * rng.random((T, 4))).astype(np.float32)
+    if kind == "strong_decay":
+        g = (-3.0 - 0.5 * rng.random((T, 4))).astype(np.float32)
+    elif kind == "no_decay":
+        g = np.zeros((T, 4), np.float32)
+    else:
+        g = np.where((np.arange(T) // 7 % 2 == 0)[:, None], -3.0, 0.0).astype(np.float32) * np.ones((1, 4), np.float32)
+    tok = wl.Tokens(tok.xq, tok.xk, tok.xv, g, beta)
+    run = Runner(shape, tok, cw, cuda_device)
+    sess, out = run.session(), run.new_out()
+    n = run.prefill(sess, 0, T, out, gdn.GDN_ALLOW_PARTIAL)
+    assert n == T
+    o_ref, ST_ref, cs_ref = oracle_run(shape, tok, cw)
+    _check(run, sess, out, n, o_ref, ST_ref, cs_ref)
