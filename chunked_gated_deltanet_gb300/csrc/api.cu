@@ -585,7 +585,7 @@ GDN_API gdn_status gdn_decode_step(const gdn_layer_desc *d, gdn_session *session
         }
         p.n_sess = cnt; p.nblk = 0;
         cudaStream_t cst = (cudaStream_t)stream;
-        cudaError_t e = launch_k(K_DECODE, cst, [&] { return gdn_launch_decode(p, D, in_bf16, ch, cst); });
+        cudaError_t e = launch_k(K_DECODE, cst, [&] { return gdn_launch_decode(p, D, in_bf16, ch, i0 / gdn::kLaunchSessions, cst); });
         if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
     }
     for (int i = 0; i < n; ++i) sessions[i].committed += 1;

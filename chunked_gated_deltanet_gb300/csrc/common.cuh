@@ -119,10 +119,10 @@ cudaError_t gdn_sm_count(int *out);
 // Launches kernel<<<grid, block, smem, st>>>(args...) with programmatic stream serialization (the kernel
 // calls grid_dep_wait before touching data of earlier work).
 template <class... K, class... A>
-cudaError_t gdn_launch_pdl(void (*kernel)(K...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+cudaError_t gdn_launch_pdl(void (*kernel)(K...), dim3 grid, unsigned block, size_t smem, cudaStream_t st,
                            A &&...args) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -146,6 +146,7 @@ cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, c
 cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *dst1, const void *src1,
                             size_t bytes1, cudaStream_t st);
-cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
+// chunk: the index of this launch among the launches of one decode call (64 sessions each)
+cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, int chunk, cudaStream_t st);
 cudaError_t gdn_launch_gates(const float *a, const float *b, const float *A_log, const float *dt_bias, int64_t n,
                              int Hv, float *g, float *beta, cudaStream_t st);

@@ -57,8 +57,14 @@ __global__ void __launch_bounds__(256) copy2_kernel(uint4 *d0, const uint4 *s0, 
 // depend on the batch. The CTA is the only reader of its channels' conv state (q and k of its head, v of
 // its v-heads), and each channel's old state is read by the one thread that writes its new state, so
 // the conv state is committed in place without a separate launch.
+// A call of more than 64 sessions is several launches (chunks) over disjoint sessions, each letting the next
+// start as its CTAs leave: chunk 0 waits for earlier work before it lets the next one launch, so every
+// chunk starts after that work; a later chunk waits for the chunk before it only at its end, so that the
+// last chunk completes after every other one and work after the call waits for the whole step.
 template <int D, typename InT>
-__global__ void __launch_bounds__(256) decode_kernel(const LaunchCommon p, int64_t ch) {
+__global__ void __launch_bounds__(256) decode_kernel(const LaunchCommon p, int64_t ch, int chunk) {
+    if (chunk == 0) grid_dep_wait();   // inputs, states and conv states, written by earlier work
+    grid_dep_launch();
     constexpr int NT = 256, LPR = D / 4, NRG = NT / LPR, RPT = D / NRG, NW = NT / 32;
     static_assert(2 * D <= NT && RPT * NRG == D, "thread map");
     __shared__ float qk[2][D], vv[D], uu[D], red[NRG][D], ss[NW];
@@ -161,6 +167,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const LaunchCommon p, int64
         }
         __syncthreads();   // red, vv and uu are read before the next head writes them
     }
+    if (chunk > 0) grid_dep_wait();   // the chunk before this one is complete
 }
 
 // g and beta from raw per-token projections (the raw-gate variant, the usual Gated-DeltaNet
@@ -208,15 +215,15 @@ cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *d
     return cudaGetLastError();
 }
 
-cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st) {
+cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, int chunk, cudaStream_t st) {
     using namespace gdn;
-    dim3 grid(p.n_sess, p.Hk);
-    if (D == 64) {
-        if (in_bf16) decode_kernel<64, __nv_bfloat16><<<grid, 256, 0, st>>>(p, ch);
-        else decode_kernel<64, float><<<grid, 256, 0, st>>>(p, ch);
-    } else {
-        if (in_bf16) decode_kernel<128, __nv_bfloat16><<<grid, 256, 0, st>>>(p, ch);
-        else decode_kernel<128, float><<<grid, 256, 0, st>>>(p, ch);
-    }
-    return cudaGetLastError();
+    const dim3 grid(p.n_sess, p.Hk);
+    cudaError_t e;
+    if (D == 64)
+        e = in_bf16 ? gdn_launch_pdl(decode_kernel<64, __nv_bfloat16>, grid, 256, 0, st, p, ch, chunk)
+                    : gdn_launch_pdl(decode_kernel<64, float>, grid, 256, 0, st, p, ch, chunk);
+    else
+        e = in_bf16 ? gdn_launch_pdl(decode_kernel<128, __nv_bfloat16>, grid, 256, 0, st, p, ch, chunk)
+                    : gdn_launch_pdl(decode_kernel<128, float>, grid, 256, 0, st, p, ch, chunk);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
