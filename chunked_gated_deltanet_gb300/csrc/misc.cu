@@ -38,9 +38,13 @@ __global__ void __launch_bounds__(256) conv_commit_kernel(const LaunchCommon p, 
     }
 }
 
-// Two independent 16-byte-vector copies in one launch; a null source zero-fills.
+// Two independent 16-byte-vector copies in one launch; a null source zero-fills. Launched with
+// programmatic stream serialization: it waits for earlier work before touching memory, then lets the next
+// kernel start as its CTAs leave.
 __global__ void __launch_bounds__(256) copy2_kernel(uint4 *d0, const uint4 *s0, size_t n0, uint4 *d1,
                                                     const uint4 *s1, size_t n1) {
+    grid_dep_wait();
+    grid_dep_launch();
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n0 + n1; i += stride) {
         if (i < n0) d0[i] = s0 ? s0[i] : make_uint4(0, 0, 0, 0);
@@ -209,10 +213,10 @@ cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *d
     if (n == 0) return cudaSuccess;
     unsigned blocks = (unsigned)((n + 255) / 256);
     if (blocks > 152u * 8u) blocks = 152u * 8u;
-    gdn::copy2_kernel<<<blocks, 256, 0, st>>>(static_cast<uint4 *>(dst0), static_cast<const uint4 *>(src0),
-                                              bytes0 / 16, static_cast<uint4 *>(dst1),
-                                              static_cast<const uint4 *>(src1), bytes1 / 16);
-    return cudaGetLastError();
+    const cudaError_t e = gdn_launch_pdl(gdn::copy2_kernel, blocks, 256, 0, st, static_cast<uint4 *>(dst0),
+                                         static_cast<const uint4 *>(src0), bytes0 / 16, static_cast<uint4 *>(dst1),
+                                         static_cast<const uint4 *>(src1), bytes1 / 16);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t gdn_launch_decode(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, int chunk, cudaStream_t st) {
