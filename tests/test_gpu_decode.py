@@ -81,3 +81,37 @@ def test_decode_one_session_many_heads_equals_batch_of_one(cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(oa[0], ob[2])
     assert torch.equal(sessA[2].S, sessB[2].S) and torch.equal(sessA[2].conv, sessB[2].conv)
+
+
+def test_decode_over_several_launches_equals_single_steps(cuda_device):
+    """A decode call over 150 sessions runs as three launches of at most 64 sessions, each letting the next
+    start early; over two consecutive steps (the second reads the states the first wrote) every session's
+    output, state and conv state equal those of single-session calls, bit for bit."""
+    dev = cuda_device
+    desc = gdn.make_desc(2, 4, 64, 64, 64, gdn.GDN_BF16, gdn.GDN_FP32)
+    n, nq, nv = 150, 2 * 64, 4 * 64
+    gen = torch.Generator(device=dev).manual_seed(11)
+    bf = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)
+    batch = [gdn.Session(desc, dev) for _ in range(n)]
+    single = [gdn.Session(desc, dev) for _ in range(n)]
+    for a, b in zip(batch, single):
+        a.S.copy_(0.1 * torch.randn(a.S.shape, generator=gen, device=dev))
+        a.conv.copy_(bf(*a.conv.shape))
+        b.S.copy_(a.S)
+        b.conv.copy_(a.conv)
+    cw = bf(2 * nq + nv, 4)
+    for _ in range(2):
+        xq, xk, xv = bf(n, nq), bf(n, nq), bf(n, nv)
+        g = -0.1 * torch.nn.functional.softplus(torch.randn(n, 4, generator=gen, device=dev))
+        beta = torch.sigmoid(torch.randn(n, 4, generator=gen, device=dev))
+        out_b = torch.zeros((n, 4, 64), device=dev)
+        gdn.gdn_decode_step(desc, batch, xq, xk, xv, g, beta, cw, out_b)
+        out_s = torch.zeros((n, 4, 64), device=dev)
+        for i in range(n):
+            gdn.gdn_decode_step(desc, [single[i]], xq[i:i + 1], xk[i:i + 1], xv[i:i + 1], g[i:i + 1], beta[i:i + 1],
+                                cw, out_s[i:i + 1])
+        torch.cuda.synchronize()
+        assert torch.equal(out_b, out_s)
+    for a, b in zip(batch, single):
+        assert torch.equal(a.S, b.S) and torch.equal(a.conv, b.conv)
+        assert a.committed == b.committed == 2
