@@ -37,6 +37,8 @@ struct LaunchCommon {
     float q_scale, eps;
     int n_sess;
     int nblk;                   // total blocks of this launch
+    int blk_lo;                 // tcgen05 prologue: > 0 runs the tasks of blocks [blk_lo, nblk) only, beside the
+                                // state pass launched before it, and waits for that one at its end (see prep_umma.cu)
     long long wait_limit;       // polls before a bounded mbarrier wait gives up
     unsigned int *err;          // device error word (bit 0: a bounded wait ran out)
     int debug_skip_first_copy;  // test hook: 1 = the state kernel, 2 = the tcgen05 prologue never issues its first copy
@@ -141,7 +143,8 @@ void gdn_internal_set_error(const char *msg);
 cudaError_t gdn_launch_prep(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_state(const gdn::LaunchCommon &p, int D, cudaStream_t st);
 cudaError_t gdn_launch_prep_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
-cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st);
+// max_ctas: at most that many CTAs (0: one per SM)
+cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st, int max_ctas = 0);
 cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *dst1, const void *src1,
