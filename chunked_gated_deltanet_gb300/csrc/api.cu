@@ -165,8 +165,9 @@ cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int6
 }
 
 // ---- optional per-kernel event timing ----
-enum Kind { K_PREP = 0, K_CONV = 1, K_STATE = 2, K_COPY = 3, K_DECODE = 4, K_GATES = 5, K_KINDS = 6 };
-const char *const kKindName[K_KINDS] = {"prep_wy", "conv_commit", "state_output", "state_copy", "decode", "gates"};
+enum Kind { K_PREP = 0, K_CONV = 1, K_STATE = 2, K_COPY = 3, K_DECODE = 4, K_GATES = 5, K_PREP_TAIL = 6, K_KINDS = 7 };
+const char *const kKindName[K_KINDS] = {"prep_wy", "conv_commit", "state_output", "state_copy", "decode", "gates",
+                                        "prep_wy_tail"};
 
 struct Timing {
     bool on = false;
@@ -449,7 +450,7 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
                 if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
                 e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_tc(pa, D, ch, cst); });
                 if (e != cudaSuccess) return cuda_fail(e, "state/output kernel");
-                e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep_umma(pt, ch, cst, free_sms); });
+                e = launch_k(K_PREP_TAIL, cst, [&] { return gdn_launch_prep_umma(pt, ch, cst, free_sms); });
                 if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
                 e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_tc(pb, D, ch, cst); });
             } else if (in_bf16) {

@@ -308,7 +308,9 @@ gdn_status gdn_gates(const gdn_layer_desc *desc, const float *a, const float *b,
  * with *n_kinds the number of kinds that launched. Process-global and not
  * thread-safe: one benchmark thread at a time. */
 typedef struct gdn_kernel_time {
-    char name[32];        /* kernel kind: prep_wy, conv_commit, state_output, state_copy, decode, gates */
+    char name[32];        /* kernel kind: prep_wy, prep_wy_tail (the prologue of a call's last blocks, run
+                             beside the state pass of its first ones), conv_commit, state_output, state_copy,
+                             decode, gates */
     int64_t launches;     /* launches while recording */
     int64_t timed;        /* launches with an event pair */
     double total_ms;      /* summed device time of the timed launches */
