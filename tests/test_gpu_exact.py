@@ -120,6 +120,39 @@ def test_varlen_equals_solo(cuda_device):
             assert _same(s.S, sess[i].S) and _same(s.conv, sess[i].conv)
 
 
+def test_two_part_call_equals_one_part_calls(cuda_device):
+    """A one-session call whose prologue would end in a partial round of SMs runs in two parts (the last
+    blocks' prologue beside the first blocks' state pass). With 16 q/k heads a 48- or 50-block call takes
+    that path on a 152-SM GPU; a varlen call of two sessions and 16-block calls do not. All give the same
+    bits, on grid with its checkpoint and with a partial final block."""
+    shape = wl.Shape(16, 16, 128, 128, 512, wl.BF16)
+    T = 3172                                     # 3,072 on grid + a 100-token tail
+    w = wl.Workload("twopart", shape, seed=12, session_lengths=[T])
+    tok, cw = w.session_tokens(0), w.conv_weights()
+    run = Runner(shape, tok, cw, cuda_device)
+    pair = Runner(shape, wl.Tokens.concat([tok, tok]), cw, cuda_device)
+    ws2 = gdn.workspace(pair.desc, 2 * T, 2, cuda_device)
+    for flags in (0, gdn.GDN_ALLOW_PARTIAL):
+        # one call (two parts where the GPU has 152 SMs), its checkpoint written by the call
+        s1, slot1, o1 = run.session(), run.session(), run.new_out()
+        n1 = gdn.gdn_prefill_chunks_checkpoint(run.desc, s1, slot1, *run.x, run.cw_t, o1, run.ws, flags=flags)
+        assert n1 == (T if flags else 3072) == s1.committed == slot1.committed
+        # the same tokens as two sessions of one varlen call (never split)
+        sv, ov = [pair.session(), pair.session()], pair.new_out()
+        nv = gdn.gdn_prefill_varlen(pair.desc, sv, [0, T, 2 * T], *pair.x, pair.cw_t, ov, ws2, flags=flags)
+        assert nv == [n1, n1]
+        for i, s in enumerate(sv):
+            assert _same(ov[i * T:i * T + n1], o1[:n1]) and _same(s.S, s1.S) and _same(s.conv, s1.conv)
+        assert _same(slot1.S, s1.S) and _same(slot1.conv, s1.conv)
+    # on grid: three 16-block calls (one part each) reach the same state and outputs
+    s3, o3 = run.session(), run.new_out()
+    for a in (0, 1024, 2048):
+        assert run.prefill(s3, a, a + 1024, o3) == 1024
+    s4, o4 = run.session(), run.new_out()
+    assert run.prefill(s4, 0, T, o4) == 3072
+    assert _same(o3[:3072], o4[:3072]) and _same(s3.S, s4.S) and _same(s3.conv, s4.conv)
+
+
 def test_interleaved_sessions_through_slots(cuda_device):
     """One working session time-shared by 3 conversations through slots equals uninterrupted runs."""
     shape = wl.Shape(2, 2, 128, 128, 64, wl.BF16)
