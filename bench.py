@@ -939,11 +939,30 @@ def main():
         print(json.dumps(line), flush=True)
 
 
+# the reference arm's whole run (warm-up and timed steps) is sized to take about this long on the host
+REFERENCE_BUDGET_S = 120.0
+
+
+def reference_sample_tokens(n_max: int, steps: int, seconds_per_token: float) -> int:
+    """Tokens per step of the reference arm: the first n_max at most, fewer (a multiple of 512, at least 512
+    unless n_max is smaller) when steps x n_max would outlast REFERENCE_BUDGET_S at the measured rate."""
+    fit = int(REFERENCE_BUDGET_S / (max(steps, 1) * max(seconds_per_token, 1e-12)))
+    return min(n_max, max(fit // 512 * 512, min(512, n_max)))
+
+
 def run_reference(args, w, rank, world):
-    """The oracle as the reference arm: rank 0 alone, host cores."""
+    """The oracle as the reference arm: rank 0 alone, host cores. Each step runs the oracle over the first
+    tokens of the session; their number is set by an untimed probe of the oracle's rate so that the whole
+    run stays within a few minutes whatever --steps and --warmup are."""
     if rank != 0:
         return
-    n = min(args.cpu_sample_tokens, w.session_lengths[0])
+    n_max = min(args.cpu_sample_tokens, w.session_lengths[0])
+    n_probe = min(2048, n_max)
+    probe = oracle_sample(w, n_probe)
+    probe()                                  # loads the oracle and starts its threads
+    t0 = time.time()
+    probe()
+    n = reference_sample_tokens(n_max, args.steps + args.warmup, (time.time() - t0) / n_probe)
     run = oracle_sample(w, n)
     for _ in range(args.warmup):
         run()

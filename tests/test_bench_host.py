@@ -73,3 +73,17 @@ def test_reference_arm_under_torchrun_prints_once():
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1
     _check_reference_line(lines[0])
+
+
+def test_reference_sample_fits_the_time_budget():
+    """The reference arm shrinks its per-step sample (multiples of 512) so that warm-up + timed steps stay
+    within its budget at the measured oracle rate, and never grows it past the requested sample."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rate = 2.4 / 41472                       # seconds per token of the whole-layer oracle on 16 cores
+    n = bench.reference_sample_tokens(41472, 103, rate)
+    assert n % 512 == 0 and 512 <= n < 41472
+    assert 103 * n * rate <= bench.REFERENCE_BUDGET_S
+    assert bench.reference_sample_tokens(41472, 6, rate) == 41472
+    assert bench.reference_sample_tokens(64, 1, 1.0) == 64
+    assert bench.reference_sample_tokens(41472, 10**6, rate) == 512
