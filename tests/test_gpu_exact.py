@@ -120,6 +120,35 @@ def test_varlen_equals_solo(cuda_device):
             assert _same(s.S, sess[i].S) and _same(s.conv, sess[i].conv)
 
 
+def test_varlen_beyond_one_launch_equals_solo(cuda_device):
+    """A varlen call over more sessions than one launch takes (64) runs as several launches; every session,
+    empty and sub-grid ones included, still equals its own solo call bit for bit."""
+    shape = wl.Shape(2, 4, 128, 128, 64, wl.BF16)
+    rng = np.random.default_rng(21)
+    lens = [int(x) for x in rng.integers(0, 300, size=70)]
+    lens[0], lens[5], lens[69] = 0, 40, 64
+    w = wl.Workload("vl70", shape, seed=22, session_lengths=[max(l, 1) for l in lens])
+    cw = w.conv_weights()
+    toks = [w.session_tokens(i).slice(0, L) for i, L in enumerate(lens)]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    run = Runner(shape, wl.Tokens.concat(toks), cw, cuda_device)
+    ws = gdn.workspace(run.desc, int(cu[-1]), len(lens), cuda_device)
+    for flags in (0, gdn.GDN_ALLOW_PARTIAL):
+        sess, out = [run.session() for _ in lens], run.new_out()
+        nc = gdn.gdn_prefill_varlen(run.desc, sess, cu, *run.x, run.cw_t, out, ws, flags=flags)
+        for i, L in enumerate(lens):
+            expect = L if flags else L // 64 * 64
+            assert nc[i] == sess[i].committed == expect
+            if L == 0:
+                assert float(sess[i].S.abs().max()) == 0.0
+                continue
+            solo = Runner(shape, toks[i], cw, cuda_device)
+            s, o = solo.session(), solo.new_out()
+            assert solo.prefill(s, 0, L, o, flags) == expect
+            assert _same(out[cu[i]:cu[i] + expect], o[:expect])
+            assert _same(s.S, sess[i].S) and _same(s.conv, sess[i].conv)
+
+
 def test_two_part_call_equals_one_part_calls(cuda_device):
     """A one-session call whose prologue would end in a partial round of SMs runs in two parts (the last
     blocks' prologue beside the first blocks' state pass). With 16 q/k heads a 48- or 50-block call takes
