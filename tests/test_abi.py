@@ -118,6 +118,27 @@ def test_prefill_refusals_mutate_nothing(lib):
     assert s.committed == 0
 
 
+def test_noalloc_refusals_before_any_device_work(lib):
+    """The no-allocation prefill refuses, on the host and before touching the GPU, a call whose scratch would
+    exceed the built-in array, and hands malformed arguments to the regular validation."""
+    d = _desc()
+    s = _fake_session(d)
+    nc = ctypes.c_int64(-7)
+    p = ctypes.c_void_p(0x100000)
+
+    def call(n_tokens, flags=0):
+        return lib.gdn_prefill_chunks_noalloc(ctypes.byref(d), ctypes.byref(s), p, p, p, p, p, p, n_tokens, flags,
+                                              p, ctypes.byref(nc), None)
+
+    need = gdn.gdn_workspace_size(d, 1024, 1)
+    assert need > gdn.GDN_NOALLOC_SCRATCH_BYTES
+    assert call(1024) == gdn.GDN_ERR_WORKSPACE
+    assert b"built-in" in lib.gdn_last_error()
+    assert call(-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(1024, flags=4) == gdn.GDN_ERR_INVALID_ARG
+    assert s.committed == 0 and nc.value == -7
+
+
 def test_varlen_refusals(lib):
     d = _desc()
     sess = (gdn.gdn_session * 2)(_fake_session(d), gdn.gdn_session(0x30000, 0x40000, 0, gdn.gdn_desc_tag(d)))
