@@ -242,3 +242,20 @@ def test_gate_call_refusals(lib):
     assert call(d, ok, -1, outs) == gdn.GDN_ERR_INVALID_ARG
     bad = gdn.make_desc(2, 3, 64, 64, 64)                                      # Hv not a multiple of Hk
     assert call(bad, ok, 8, outs) != gdn.GDN_OK
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No fallback: without the built library the binding raises instead of computing anything."""
+    with pytest.raises(ImportError):
+        gdn.load_library(str(tmp_path / "libgdn.so"))
+
+
+def test_product_package_never_uses_the_oracle():
+    """The oracle is test infrastructure: nothing in the package imports, loads or names its module."""
+    pkg = os.path.join(ROOT, "chunked_gated_deltanet_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "gdn_oracle" not in text, f
