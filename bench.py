@@ -39,6 +39,11 @@ if ROOT not in sys.path:
 
 METRIC = "GDN prefill tokens/s per layer on 1 GB300 + % of tensor-pipe/HBM roofline"
 UNIT = "tokens/s"
+# the arithmetic of the bf16-input path: what each stage computes in
+PRECISION = {"inputs": "bf16", "conv_norm_gates": "fp32",
+             "prologue_products": "tcgen05 kind::f16 on bf16 hi/lo operand pairs (hi*hi + hi*lo + lo*hi), fp32 accumulate",
+             "triangular_inverse": "fp32 substitution + split-tf32 products",
+             "state_pass_products": "tf32 operands, fp32 accumulate", "state": "fp32", "outputs": "fp32"}
 FALLBACK_HBM_GBS = 6800.0
 
 # Algorithmic HBM bytes per token of the fused layer: q and k per q/k head
@@ -530,6 +535,98 @@ class LongStep:
                 "outputs": "fp32", "l2": "inputs larger than L2", "parallelism": "replicas"}
 
 
+class SmallStep:
+    """The small fp32 layer (T = 2,048, 2 heads, d = 64, grid 64): one call from a zero state."""
+
+    def __init__(self, w, device):
+        import torch
+        from chunked_gated_deltanet_gb300 import gdn
+        from chunked_gated_deltanet_gb300 import workloads as wl
+        self.gdn, self.w = gdn, w
+        sh = w.shape
+        self.desc = gdn.make_desc(sh.n_qk_heads, sh.n_v_heads, sh.d_k, sh.d_v, sh.grid_c, gdn.GDN_FP32, gdn.GDN_FP32)
+        T = w.session_lengths[0]
+        self.x = wl.tokens_to_torch(w.session_tokens(0), sh.dtype, device)
+        self.cw = wl.to_torch(w.conv_weights(), sh.dtype, device)
+        self.out = torch.empty((T, sh.n_v_heads, sh.d_v), dtype=torch.float32, device=device)
+        self.ws = gdn.workspace(self.desc, T, 1, device)
+        self.sess = gdn.Session(self.desc, device)
+        self.tokens_per_step = T
+        self.block_steps_per_step = -(-T // 64)
+
+    def step(self):
+        g = self.gdn
+        g.gdn_session_init(self.desc, self.sess)
+        assert g.gdn_prefill_chunks(self.desc, self.sess, *self.x, self.cw, self.out, self.ws) == self.tokens_per_step
+
+    def config(self):
+        sh = self.w.shape
+        return {"workload": self.w.name, "sessions": 1, "session_tokens": self.tokens_per_step, "calls": 1,
+                "n_qk_heads": sh.n_qk_heads, "n_v_heads": sh.n_v_heads, "d_k": sh.d_k, "d_v": sh.d_v,
+                "grid_c": sh.grid_c, "inputs": "fp32", "state": "fp32", "outputs": "fp32",
+                "l2": "inputs smaller than L2 (the whole layer is 2,048 tokens)", "parallelism": "replicas"}
+
+
+def kernel_split(ktimes: dict, steps: int) -> dict:
+    return {k: {"launches_per_step": v[0] / steps, "ms_per_step": round(v[2] / steps, 4),
+                "share": round(v[2] / max(sum(x[2] for x in ktimes.values()), 1e-12), 4)} for k, v in ktimes.items()}
+
+
+def measure_step(step, steps: int, warmup: int):
+    """Device time of `steps` steps (CUDA events on the current stream, after `warmup` steps), then the same
+    steps again with an event pair around every launch for the per-kernel split."""
+    import torch
+    from chunked_gated_deltanet_gb300 import gdn
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step.step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    gdn.gdn_timing_begin(100_000)
+    for _ in range(steps):
+        step.step()
+    torch.cuda.synchronize()
+    return ms, gdn.gdn_timing_end()
+
+
+def other_config_measure(name: str, w, dev, steps: int, warmup: int = 3) -> dict:
+    """Tokens/s, HBM roofline fractions (step and dominant kernel) and the kernel split of one of the other
+    workloads, in the line of the headline one."""
+    cls = {"varlen8": VarlenStep, "long_session": LongStep, "small_fp32": SmallStep}[name]
+    step = cls(w, dev)
+    ms, kt = measure_step(step, steps, warmup)
+    sh = w.shape
+    in_b = 2 if sh.dtype == "bf16" else 4
+    bpt = algorithmic_bytes_per_token(sh.n_qk_heads, sh.n_v_heads, sh.d_k, in_b, 4)
+    peak, peak_src = measured_peaks()
+    rt = dict(kt)
+    if "prep_wy_tail" in rt and "prep_wy" in rt:
+        a, b = rt.pop("prep_wy_tail"), rt["prep_wy"]
+        rt["prep_wy"] = (a[0] + b[0], a[1] + b[1], a[2] + b[2])
+    prefill = {k: v for k, v in rt.items() if k in ("prep_wy", "state_output")}
+    dom_name, (launches, timed, tot) = max(prefill.items(), key=lambda kv: kv[1][2])
+    tokens_per_launch = step.tokens_per_step / (launches / steps)
+    avg_ms = tot / max(timed, 1)
+    ms_step = ms / steps
+    out = {"config": step.config(), "steps": steps, "warmup": warmup, "ms_per_step": round(ms_step, 4),
+           "tokens_per_step": step.tokens_per_step, "value": round(step.tokens_per_step / (ms_step / 1e3), 1),
+           "unit": UNIT, "algorithmic_bytes_per_token": bpt,
+           "step_frac": round(bpt * step.tokens_per_step / (ms_step / 1e3) / 1e9 / peak, 4),
+           "dominant_kernel": {"kernel": dom_name, "avg_launch_ms": round(avg_ms, 4),
+                               "frac": round(bpt * tokens_per_launch / (avg_ms / 1e3) / 1e9 / peak, 4)},
+           "peak_gbs": peak, "peak_source": peak_src, "kernels": kernel_split(kt, steps),
+           "gpu_launches_per_step": sum(v[0] for v in kt.values()) / steps}
+    if "state_output" in kt:
+        out["state_pass_us_per_block_step"] = round(kt["state_output"][2] * 1e3 / (step.block_steps_per_step * steps), 3)
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Batched decode (one token for each of n sessions), captured once in a CUDA graph
 # ---------------------------------------------------------------------------
@@ -783,6 +880,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode and branch measurements")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the other workloads' lines (8-session batch, 100k session, small fp32 layer)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=41472)
     ap.add_argument("--oracle-one-thread", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--workload", choices=["replay", "varlen8", "long_session"], default="replay",
@@ -808,8 +907,8 @@ def main():
     dev = torch.device("cuda", local)
     gdn.load_library()
     step = {"replay": ReplayStep, "varlen8": VarlenStep, "long_session": LongStep}[args.workload](w, dev)
-    if args.workload != "replay":   # the e2e, decode and branch figures belong to the headline workload
-        args.no_e2e = args.no_decode = True
+    if args.workload != "replay":   # the e2e, decode, branch and other-config figures belong to the headline run
+        args.no_e2e = args.no_decode = args.no_other_configs = True
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -840,6 +939,7 @@ def main():
     ktimes = gdn.gdn_timing_end()
     clocks = clk.stop()
     ms_max, tokens_all = reduce_max_sum(ms, step.tokens_per_step * args.steps)
+    config = step.config()
     value = tokens_all / (ms_max / 1e3)
 
     # --- end to end through host buffers ---
@@ -916,12 +1016,22 @@ def main():
 
     decode = None if args.no_decode else [decode_measure(w, dev, n) for n in (1, 256)]
     branches = None if args.no_decode else branches_measure(dev)
+    # the other workloads of the same layer family, each timed as the headline one (a few steps each)
+    others = None
+    if not args.no_other_configs:
+        del step
+        torch.cuda.empty_cache()
+        others = {}
+        for name, fn, k in (("varlen8", wl.varlen8, 10), ("long_session", wl.long_session, 10),
+                            ("small_fp32", wl.small_fp32, 200)):
+            others[name] = other_config_measure(name, fn(), dev, k)
+            torch.cuda.empty_cache()
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": step.config(),
-            "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline, "kernels": kernels, "clocks": clocks,
-            "state_pass": state_pass, "decode": decode, "branches": branches}
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "precision": PRECISION, "data": "synthetic",
+            "config": config, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roofline, "kernels": kernels,
+            "clocks": clocks, "state_pass": state_pass, "decode": decode, "branches": branches, "configs": others}
 
     # --- CPU baseline (oracle), rank 0 at N=1 only ---
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -60,7 +60,11 @@ extern "C" __attribute__((visibility("default"))) gdn_status gdn_prefill_chunks_
     if (n_tokens < 0 || (flags & ~GDN_ALLOW_PARTIAL))   // let the regular validation report it
         return gdn_prefill_chunks(desc, session, xq, xk, xv, g, beta, conv_w, n_tokens, flags, out, n_consumed,
                                   nullptr, 0, stream);
-    // size limit, checked before any CUDA call
+    // Size limit, checked before any CUDA call. gdn_workspace_size(desc, n, 1) counts ceil(n / 64) blocks
+    // plus one spare block per launch. The prefill's own check counts ceil(n / 64) blocks for this call,
+    // because a call's 64-token blocks start at its first token whether or not the session sits on the
+    // grid (a partial call after an off-grid commit included), so a call that passes this check passes that
+    // one with the spare block to spare.
     const int64_t processed = (flags & GDN_ALLOW_PARTIAL) ? n_tokens : n_tokens / desc->grid_c * desc->grid_c;
     const size_t need = gdn_workspace_size(desc, processed, 1);
     if (processed > 0 && need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) {

@@ -18,7 +18,7 @@ import torch
 
 from chunked_gated_deltanet_gb300 import gdn
 from chunked_gated_deltanet_gb300 import workloads as wl
-from helpers import Runner, desc_of
+from helpers import TOL, Runner, conv_as_f64, desc_of, oracle_run, out_rel, rel_l2_max
 
 pytestmark = pytest.mark.gpu
 
@@ -298,6 +298,23 @@ def test_shared_prefix_branches_equal_full_pass(cuda_device):
     _, res2 = _shared_prefix_run(w, cw, cuda_device, reverse=True)
     for k, v in res.items():
         assert _same(v[2], res2[k][2]) and _same(v[3], res2[k][3])
+
+
+def test_shared_prefix_branches_match_oracle(cuda_device):
+    """The shared-prefix workload's own data (request prefix 1,000 cut to 960; groups 0/1/70/128; 4 branches
+    each; grid 64; 16 heads, d = 128) against the oracle: each branch's outputs from its cut onward, its
+    final state and its conv state, every head, against one oracle pass over the branch's full prompt."""
+    w = wl.shared_prefix()
+    cw = w.conv_weights()
+    _, res = _shared_prefix_run(w, cw, cuda_device)
+    tol_o, tol_s = TOL[w.shape.dtype]
+    assert len(res) == 16
+    for (g, b), (bt, gcut, ob, S, conv) in res.items():
+        o_ref, ST_ref, cs_ref = oracle_run(w.shape, bt, cw)
+        r_o = out_rel(ob.double().cpu().numpy(), o_ref[gcut:])
+        r_s = rel_l2_max(S.double().cpu().numpy(), ST_ref)
+        assert r_o <= tol_o and r_s <= tol_s, ((g, b), r_o, r_s)
+        assert np.array_equal(conv_as_f64(conv), cs_ref), (g, b)
 
 
 def test_branches_in_one_call_equal_restore_and_prefill(cuda_device):

@@ -1,14 +1,18 @@
 """Full-size workloads through the C ABI: bit-exact structure checks on every
-row, and oracle parity on sampled heads (heads are independent, so a subset
-of heads is exactly what the oracle computes for them).
+row, and oracle parity on every head of every session (the oracle runs over
+groups of v-heads, which is exactly what it computes for the whole layer: heads
+are independent, and each group carries the q/k heads it reads).
 
 * Qwen3.5-0.8B-shaped replay: 41,802 tokens in 30 turns, grid 512, held tail;
-  replay == fresh bit for bit, then the fork of the bench step.
+  replay == fresh bit for bit, then the fork of the bench step; all 16 heads
+  against the oracle over every row, the fork's state and the conv state.
 * varlen batch of 8 sessions (Hk 16, Hv 32, grid 512) in 6 turn rounds with a
-  checkpoint slot per session and round; varlen == solo bit for bit.
+  checkpoint slot per session and round; varlen == solo bit for bit; every
+  session's committed rows, final state and conv state against the oracle.
 * long session of 100,000 tokens (Hk 16, Hv 32, slow decay) in 6 turns with 6
   slots, then 64 forks of 20..200 question tokens; every fork restores the
-  committed state bit for bit and equals a full pass of (session + question).
+  committed state bit for bit and equals a full pass of (session + question);
+  all 32 heads against the oracle on the committed session and two forks.
 """
 import numpy as np
 import pytest
@@ -26,15 +30,39 @@ def _same(a, b):
     return torch.equal(a, b)
 
 
-def _sampled_parity(shape, tok, cw, v_heads, out_rows, S_gpu, conv_gpu=None, ST0=None, cs0=None):
-    o_ref, ST_ref, cs_ref = oracle_run(shape, tok, cw, v_heads=v_heads, ST0=ST0, conv_state=cs0)
+def _head_groups(sh, size=16):
+    """v-heads in groups of `size` (whole GQA groups), so that one oracle call holds a bounded slice of the
+    layer while its threads still run one head each."""
+    size = max(sh.n_v_heads // sh.n_qk_heads, min(size, sh.n_v_heads))
+    return [list(range(a, min(a + size, sh.n_v_heads))) for a in range(0, sh.n_v_heads, size)]
+
+
+def _parity(shape, tok, cw, out_rows, S_gpu, conv_gpu=None, ST0=None, cs0=None, act=0, q_scale=1.0):
+    """Every v-head against the oracle: outputs over every row, the final state, and (given) the conv state,
+    which holds raw inputs and must match exactly. Returns the oracle's final state [Hv, dk, dv] and conv
+    state [3, ch] over all heads, the starting point of a continuation."""
+    import oracle
     tol_o, tol_s = TOL[shape.dtype]
-    o = out_rows[:, v_heads].double().cpu().numpy()
-    r_o = out_rel(o, o_ref)
-    r_s = rel_l2_max(S_gpu[v_heads].double().cpu().numpy(), ST_ref)
-    assert r_o <= tol_o, r_o
-    assert r_s <= tol_s, r_s
-    return o_ref, ST_ref, cs_ref
+    Hk, Hv, dk, dv = shape.n_qk_heads, shape.n_v_heads, shape.d_k, shape.d_v
+    ST_all = np.zeros((Hv, dk, dv))
+    cs_all = np.zeros((3, shape.channels))
+    nq = Hk * dk
+    worst_o = worst_s = 0.0
+    for vh in _head_groups(shape):
+        o_ref, ST_ref, cs_ref = oracle_run(shape, tok, cw, v_heads=vh, ST0=ST0, conv_state=cs0, act=act,
+                                           q_scale=q_scale)
+        worst_o = max(worst_o, out_rel(out_rows[:, vh].double().cpu().numpy(), o_ref))
+        worst_s = max(worst_s, rel_l2_max(S_gpu[vh].double().cpu().numpy(), ST_ref))
+        _, qk_cols, v_cols = oracle.head_columns(Hk, Hv, dk, dv, vh)
+        chan = np.concatenate([qk_cols, nq + qk_cols, 2 * nq + v_cols])
+        ST_all[vh] = ST_ref
+        cs_all[:, chan] = cs_ref
+        del o_ref
+    assert worst_o <= tol_o, worst_o
+    assert worst_s <= tol_s, worst_s
+    if conv_gpu is not None:
+        assert np.array_equal(conv_as_f64(conv_gpu), cs_all)
+    return ST_all, cs_all
 
 
 def test_qwen08b_replay_full(cuda_device):
@@ -67,8 +95,9 @@ def test_qwen08b_replay_full(cuda_device):
     full = run.session()
     run.prefill(full, 0, len(tok), o_fresh, gdn.GDN_ALLOW_PARTIAL)
     assert _same(o_rep[n:], o_fresh[n:]) and _same(S_fork, full.S)
-    # parity against the oracle on two sampled heads over every row
-    _sampled_parity(w.shape, tok, cw, [0, 11], o_fresh, full.S)
+    # every head against the oracle over every row (committed rows and the fork's), the fork's final state
+    # and its conv state
+    _parity(w.shape, tok, cw, o_fresh, full.S, full.conv)
 
 
 def test_varlen8_full(cuda_device):
@@ -118,10 +147,10 @@ def test_varlen8_full(cuda_device):
     f, of = runs[i].session(), runs[i].new_out()
     n = runs[i].prefill(f, 0, lens[i], of)
     assert _same(of[:n], outs[i][:n]) and _same(f.S, sess[i].S)
-    # oracle parity: shortest session, one GQA group (v-heads 6, 7 read q/k head 3)
-    j = int(np.argmin(lens))
-    n = sess[j].committed
-    _sampled_parity(sh, toks[j].slice(0, n), cw, [6, 7], outs[j][:n], sess[j].S)
+    # oracle parity: every session's committed rows, final state and conv state, all 32 heads
+    for j in range(8):
+        n = sess[j].committed
+        _parity(sh, toks[j].slice(0, n), cw, outs[j][:n], sess[j].S, sess[j].conv)
 
 
 def test_long_session_forks_full(cuda_device):
@@ -166,31 +195,11 @@ def test_long_session_forks_full(cuda_device):
         assert _same(fo, of[committed:T + q]) and _same(S_fork, full.S), j
         if j in (0, 1):
             checked[j] = (qt, fo.clone(), S_fork)
-    # oracle parity: one GQA group over the committed session, then two forks continuing from it
-    vh = [30, 31]
-    o_ref, ST_ref, cs_ref = _sampled_parity(sh, tok.slice(0, committed), cw, vh, out[:committed], S0)
+    # oracle parity, all 32 heads: the committed session, then two forks continuing from it
+    ST_ref, cs_ref = _parity(sh, tok.slice(0, committed), cw, out[:committed], S0, c0)
     tail = tok.slice(committed, T)
     for j, (qt, fo, S_fork) in checked.items():
-        _sampled_parity(sh, wl.Tokens.concat([tail, qt]), cw, vh, fo, S_fork,
-                        ST0=_embed(ST_ref, vh, sh), cs0=_embed_conv(cs_ref, vh, sh))
-
-
-def _embed(ST_sub, v_heads, sh):
-    ST = np.zeros((sh.n_v_heads, sh.d_k, sh.d_v))
-    ST[v_heads] = ST_sub
-    return ST
-
-
-def _embed_conv(cs_sub, v_heads, sh):
-    """Place the sampled heads' conv-state columns back into a full [3, ch] array."""
-    import oracle
-    Hk, Hv, dk, dv = sh.n_qk_heads, sh.n_v_heads, sh.d_k, sh.d_v
-    _, qk_cols, v_cols = oracle.head_columns(Hk, Hv, dk, dv, v_heads)
-    nq = Hk * dk
-    chan = np.concatenate([qk_cols, nq + qk_cols, 2 * nq + v_cols])
-    cs = np.zeros((3, sh.channels))
-    cs[:, chan] = cs_sub
-    return cs
+        _parity(sh, wl.Tokens.concat([tail, qt]), cw, fo, S_fork, ST0=ST_ref, cs0=cs_ref)
 
 
 def test_grid_2048_replay_and_grid_independence(cuda_device):
@@ -217,15 +226,11 @@ def test_grid_2048_replay_and_grid_independence(cuda_device):
 
 
 def test_silu_and_q_scale_on_the_replay(cuda_device):
-    """The replay tokens with the SiLU conv and q scaled by d^-1/2: oracle parity on sampled heads."""
+    """The replay tokens with the SiLU conv and q scaled by d^-1/2: every head against the oracle."""
     w = wl.qwen08b_replay()
     tok, cw = w.session_tokens(0), w.conv_weights()
     qs = float(w.shape.d_k) ** -0.5
     run = Runner(w.shape, tok, cw, cuda_device, act=gdn.GDN_CONV_SILU, q_scale=qs)
     sess, out = run.session(), run.new_out()
     n = run.prefill(sess, 0, len(tok), out)
-    heads = [5, 14]
-    o_ref, ST_ref, _ = oracle_run(w.shape, tok.slice(0, n), cw, v_heads=heads, act=1, q_scale=qs)
-    tol_o, tol_s = TOL[w.shape.dtype]
-    assert out_rel(out[:n][:, heads].double().cpu().numpy(), o_ref) <= tol_o
-    assert rel_l2_max(sess.S[heads].double().cpu().numpy(), ST_ref) <= tol_s
+    _parity(w.shape, tok.slice(0, n), cw, out[:n], sess.S, sess.conv, act=1, q_scale=qs)
