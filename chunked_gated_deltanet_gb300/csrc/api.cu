@@ -115,7 +115,8 @@ WsLayout ws_layout(const gdn_layer_desc *d, int64_t nblk) {
     if (d->in_dtype == GDN_BF16) {  // tensor-core path: one record per (block, v-head)
         L.qk_off = 0;
         L.wu_off = 0;
-        L.bytes = kWsAlign + align256((size_t)nblk * d->n_v_heads * gdn::rec_floats(D) * sizeof(float));
+        const size_t rec = D == 128 ? gdn::rec16::kBytes : gdn::rec_floats(D) * sizeof(float);
+        L.bytes = kWsAlign + align256((size_t)nblk * d->n_v_heads * rec);
         return L;
     }
     L.qk_off = 0;
@@ -293,16 +294,18 @@ namespace {
 // receives its own result, as if the prefix had been restored into it first.
 // Where to split a one-session bf16 launch (d = 128) whose prologue would end with a partial round: blocks
 // [0, split) take whole rounds of one CTA per SM, and the tasks of the rest run, on the SMs the state pass
-// of the first part leaves (one CTA per SM for each of its 16-column chains), while that state pass runs.
-// 0: no split (no partial round, no free SMs, or the rest would outlast the first state pass). The times
-// are those measured on GB300 for this layer: about 12.5 us per prologue task (one q/k head of a
-// 64-token block) and 1.4 us per state step, plus about 5 us of fixed state-pass cost, which the second
-// state pass adds.
+// of the first part leaves (its chain CTAs hold one SM each), while that state pass runs. 0: no split (no
+// partial round, no free SMs, or the rest would outlast the first state pass). The times are those
+// measured on GB300 for this layer: about 12.5 us per round of prologue tasks (one q/k head of a 64-token
+// block per SM) and, for the state pass, kStateStepUs per block plus kStateFixedUs per launch, which the
+// second state pass adds.
+constexpr double kPrologueRoundUs = 12.5, kStateStepUs = 0.6, kStateFixedUs = 4.0;
 static int tail_split(const LaunchCommon &p, const gdn_layer_desc *d) {
     if (p.n_sess != 1 || p.G != 1) return 0;
     int sms = 0;
     if (gdn_sm_count(&sms) != cudaSuccess) return 0;
-    const int Hk = p.Hk, nblk = p.nblk, nchain = d->n_v_heads * (d->d_v / gdn::kSliceCols);
+    const int Hk = p.Hk, nblk = p.nblk;
+    const int nchain = d->n_v_heads * (d->d_v / gdn_chain_umma_cols(d->n_v_heads, sms));
     const int free_sms = sms - nchain;
     if (nchain > sms || free_sms < 8) return 0;
     const int64_t ntask = (int64_t)nblk * Hk, rounds = (ntask + sms - 1) / sms;
@@ -310,8 +313,9 @@ static int tail_split(const LaunchCommon &p, const gdn_layer_desc *d) {
     const int split = (int)((rounds - 1) * sms / Hk);   // blocks in whole rounds
     if (split < 1 || split >= nblk) return 0;
     const int64_t rest = (int64_t)(nblk - split) * Hk, rest_rounds = (rest + free_sms - 1) / free_sms;
-    const double t_rest = 12.5 * (double)rest_rounds, t_first_state = 1.4 * split + 3.5;
-    return t_rest <= t_first_state ? split : 0;   // a round saved (12.5 us) against a second state pass (5 us)
+    const double t_rest = kPrologueRoundUs * (double)rest_rounds, t_first_state = kStateStepUs * split + kStateFixedUs;
+    // a round saved against a second state pass's fixed cost
+    return t_rest <= t_first_state && kPrologueRoundUs > kStateFixedUs ? split : 0;
 }
 
 gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t n_sessions, const int64_t *cu,
@@ -445,19 +449,23 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
                 pb.nblk = p.nblk - split;
                 int sms = 0;
                 if ((e = gdn_sm_count(&sms)) != cudaSuccess) return cuda_fail(e, "SM count");
-                const int free_sms = sms - d->n_v_heads * (D / gdn::kSliceCols);
+                const int cols = gdn_chain_umma_cols(d->n_v_heads, sms);
+                const int free_sms = sms - d->n_v_heads * (D / cols);
                 e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep_umma(pa, ch, cst); });
                 if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
-                e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_tc(pa, D, ch, cst); });
+                e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_umma(pa, ch, cst, cols); });
                 if (e != cudaSuccess) return cuda_fail(e, "state/output kernel");
                 e = launch_k(K_PREP_TAIL, cst, [&] { return gdn_launch_prep_umma(pt, ch, cst, free_sms); });
                 if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
-                e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_tc(pb, D, ch, cst); });
+                e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_umma(pb, ch, cst, cols); });
             } else if (in_bf16) {
-                // bf16 inputs: tf32 tensor-core kernels; the state kernel also commits the conv state
+                // bf16 inputs: tensor-core kernels (d = 128: tcgen05 prologue and state pass over fp16 records;
+                // d = 64: the warp-level ones); the state kernel also commits the conv state
                 e = launch_k(K_PREP, cst, [&] { return D == 128 ? gdn_launch_prep_umma(p, ch, cst) : gdn_launch_prep_tc(p, D, ch, cst); });
                 if (e != cudaSuccess) return cuda_fail(e, "prologue/WY kernel");
-                e = launch_k(K_STATE, cst, [&] { return gdn_launch_chain_tc(p, D, ch, cst); });
+                e = launch_k(K_STATE, cst, [&] {
+                    return D == 128 ? gdn_launch_chain_umma(p, ch, cst) : gdn_launch_chain_tc(p, D, ch, cst);
+                });
             } else {
                 // fp32 inputs: fp32 kernels (tighter tolerance)
                 e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep(p, D, in_bf16, ch, cst); });

@@ -78,6 +78,27 @@ __device__ __forceinline__ int cfrag_slice_index(int i, int c) {
     return ((((sl * 4 + (i >> 4)) * 2 + (cc >> 3)) * 32 + lane) * 4 + f);
 }
 
+// fp16 record of the tcgen05 path (bf16 inputs, d_k = d_v = 128), one per (64-token block, v-head), written
+// by the prologue in the layouts the tcgen05 state pass reads straight from shared memory. Offsets in bytes.
+// A core matrix is 8 rows x 16 bytes (8 fp16), stored as 128 contiguous bytes.
+namespace rec16 {
+constexpr uint32_t kWQ = 0;         // [W; Qe], 128 x 128: A operand of [W; Qe] S^T, K-major cores, LBO 128 (along K),
+                                    // SBO 2048 (along M)
+constexpr uint32_t kKT = 32768;     // K_tilde^T, 128 (d_k) x 64 (tokens): A operand of K_tilde^T U', K-major cores,
+                                    // LBO 128, SBO 1024
+constexpr uint32_t kU = 49152;      // U, 64 x 128, as [column / 8][row][column % 8]: 1 KB per 8 columns
+constexpr uint32_t kO = 65536;      // O_intra, the same layout
+constexpr uint32_t kEg = 81920;     // e^{gamma_63} (fp32)
+constexpr uint32_t kBytes = 82048;  // the record's stride (a multiple of 128 bytes)
+__host__ __device__ constexpr uint32_t wq(int r, int k) {
+    return (uint32_t)(r >> 3) * 2048u + (uint32_t)(k >> 3) * 128u + (uint32_t)(r & 7) * 16u + (uint32_t)(k & 7) * 2u;
+}
+__host__ __device__ constexpr uint32_t kt(int d, int j) {
+    return kKT + (uint32_t)(d >> 3) * 1024u + (uint32_t)(j >> 3) * 128u + (uint32_t)(d & 7) * 16u + (uint32_t)(j & 7) * 2u;
+}
+__host__ __device__ constexpr uint32_t uo(int i, int c) { return (uint32_t)(c >> 3) * 1024u + (uint32_t)i * 16u + (uint32_t)(c & 7) * 2u; }
+}  // namespace rec16
+
 template <typename T> __device__ __forceinline__ float to_f(T x);
 template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -146,6 +167,10 @@ cudaError_t gdn_launch_prep_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cu
 // max_ctas: at most that many CTAs (0: one per SM)
 cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st, int max_ctas = 0);
 cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
+// The tcgen05 state pass over fp16 records (d = 128); cols: d_v columns per CTA (32, 64 or 128; 0 chooses by the
+// launch's chain count, gdn_chain_umma_cols)
+cudaError_t gdn_launch_chain_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st, int cols = 0);
+int gdn_chain_umma_cols(int n_chains_of_128, int sms);
 cudaError_t gdn_launch_conv_commit(const gdn::LaunchCommon &p, int D, int in_bf16, int64_t ch, cudaStream_t st);
 cudaError_t gdn_launch_copy(void *dst0, const void *src0, size_t bytes0, void *dst1, const void *src1,
                             size_t bytes1, cudaStream_t st);

@@ -112,55 +112,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 // the two bf16 values of a 32-bit word as an fp32 pair (low half first)
 __device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t u) { return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u)); }
 
-// dst[0] = a, dst[1] = b in one 32-byte store (dst 32-byte aligned)
-__device__ __forceinline__ void st_v8(float4 *dst, float4 a, float4 b) {
-    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"l"(dst), "f"(a.x), "f"(a.y), "f"(a.z), "f"(a.w),
-                 "f"(b.x), "f"(b.y), "f"(b.z), "f"(b.w)
-                 : "memory");
-}
-
-// Each thread of a warp holds row r (r % 16 == lane % 16) of a 16-column chunk
-// starting at column c0 (a multiple of 16). The pair of lanes (l, l ^ 8)
-// holds rows r and r ^ 8 and together writes their m16n8k8 A fragments
-// (float4 per fragment lane) of an operand with K columns: each thread the
-// two adjacent fragment lanes L, L + 1 (L even) in one 32-byte store, so that a
-// store instruction fills whole sectors.
-__device__ __forceinline__ void put_afrag16(float *base, int r, int c0, const float (&v)[16], int K, int lane) {
-    const bool upper = lane & 8;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const float *w = v + 8 * h;
-        const float p0 = __shfl_xor_sync(0xffffffffu, upper ? w[0] : w[2], 8);
-        const float p1 = __shfl_xor_sync(0xffffffffu, upper ? w[1] : w[3], 8);
-        const float p2 = __shfl_xor_sync(0xffffffffu, upper ? w[4] : w[6], 8);
-        const float p3 = __shfl_xor_sync(0xffffffffu, upper ? w[5] : w[7], 8);
-        const float4 f0 = upper ? make_float4(p0, w[2], p2, w[6]) : make_float4(w[0], p0, w[4], p2);
-        const float4 f1 = upper ? make_float4(p1, w[3], p3, w[7]) : make_float4(w[1], p1, w[5], p3);
-        const int L = 4 * (r & 7) + (upper ? 2 : 0), ks = (c0 >> 3) + h;
-        float4 *dst = reinterpret_cast<float4 *>(base) + (((r >> 4) * (K >> 3) + ks) * 32 + L);
-        st_v8(dst, f0, f1);
-    }
-}
-
-// Same pairing, for row i of a 64 x D accumulator stored by 16-column slices
-// of m16n8 C fragments (cfrag_slice_index order).
-__device__ __forceinline__ void put_cfrag16(float *base, int i, int c0, const float (&v)[16], int lane) {
-    const bool upper = lane & 8;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const float *w = v + 8 * h;
-        const float p0 = __shfl_xor_sync(0xffffffffu, upper ? w[0] : w[4], 8);
-        const float p1 = __shfl_xor_sync(0xffffffffu, upper ? w[1] : w[5], 8);
-        const float p2 = __shfl_xor_sync(0xffffffffu, upper ? w[2] : w[6], 8);
-        const float p3 = __shfl_xor_sync(0xffffffffu, upper ? w[3] : w[7], 8);
-        const float4 f0 = upper ? make_float4(p0, p1, w[4], w[5]) : make_float4(w[0], w[1], p0, p1);
-        const float4 f1 = upper ? make_float4(p2, p3, w[6], w[7]) : make_float4(w[2], w[3], p2, p3);
-        const int L = 4 * (i & 7) + (upper ? 2 : 0);
-        float4 *dst = reinterpret_cast<float4 *>(base) + ((((c0 >> 4) * 4 + (i >> 4)) * 2 + h) * 32 + L);
-        st_v8(dst, f0, f1);
-    }
-}
-
 // x = hi + lo exactly, hi the tf32 truncation of x (low 13 bits cleared), lo the rest in fp32. The MMA
 // reads lo as tf32 by dropping its low 13 bits, so a split product misses at most about 2^-20 |x| of each
 // operand: far below the bf16 hi/lo split (about 2^-16) that the inverse's result goes through next.
@@ -556,27 +507,27 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             gates_store(ghead);
             if (!(ok = wait_in())) break;
         }
-        float *rec = p.ws_wu + ((int64_t)blk * Hv + h) * rec_floats(D);
-        // K_tilde^T as tf32 A fragments (D x 64), half `part` of its float4 groups, by warps 1-15 (warp 0
-        // issues the MMAs); e^{gamma_63} with the first half
+        unsigned char *rec = reinterpret_cast<unsigned char *>(p.ws_wu) + ((int64_t)blk * Hv + h) * rec16::kBytes;
+        // K_tilde^T as the fp16 K-major A operand (d_k x 64 tokens), half `part` of its 1,024 16-byte rows (row
+        // (d, tokens 8 jg .. 8 jg + 7)), by warps 1-15 (warp 0 issues the MMAs); e^{gamma_63} with the first half
         auto kt_record = [&](int part) {
             if (warp == 0) return;
-            constexpr int NG = (D / 16) * 8 * 32, HALF = NG / 2;
+            constexpr int HALF = 512;
             const float gl = gam[kBlock - 1];
             for (int e = HALF * part + t - 32; e < HALF * (part + 1); e += kUmmaPrepThreads - 32) {
-                const int ln = e & 31, tile = e >> 5, mt = tile >> 3, ks = tile & 7, gg = ln >> 2, tt = ln & 3;
-                float v[4];
+                const int d = e & (D - 1), jg = e >> 7;
+                float v[8];
 #pragma unroll
-                for (int f = 0; f < 4; ++f) {
-                    const int m = 16 * mt + gg + 8 * (f & 1), k = 8 * ks + tt + 4 * (f >> 1);
-                    const uint32_t o = kmajor_bf16_offset(kBlock + k, m, AQ_LBO, AQ_SBO);
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = 8 * jg + jj;
+                    const uint32_t o = kmajor_bf16_offset(kBlock + j, d, AQ_LBO, AQ_SBO);
                     const float kh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQh + o)) +
                                      __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQl + o));
-                    v[f] = tf32_round(__expf(gl - gam[k]) * kh);
+                    v[jj] = __expf(gl - gam[j]) * kh;
                 }
-                *reinterpret_cast<float4 *>(rec + 128 * D + e * 4) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<uint4 *>(rec + rec16::kt(d, 8 * jg)) = f8_to_h8(v);
             }
-            if (part == 0 && t == 32) rec[320 * D] = expf(gl);
+            if (part == 0 && t == 32) *reinterpret_cast<float *>(rec + rec16::kEg) = expf(gl);
         };
 
         // 5. B operand, MN-major: channels 128..255 = beta v, channels 0..127 = beta e^gamma k_hat; for the
@@ -753,9 +704,9 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             }
         }
         // 11. the record, every warp (lanes 32 (warp % 4) .., the 16-column chunks warp / 4 + 4 j, j = 0..3: two of
-        //     [W; P W] and two of [U; P U], so that every warp has the same share of the costlier first kind):
-        //     W rows -> tf32 A fragments (rows 0..63 of [W; Qe]); U rows -> C fragments;
-        //     P W rows -> Qe = e^gamma q_hat - P W (rows 64..127 of [W; Qe]); P U rows -> O_intra C fragments
+        //     [W; P W] and two of [U; P U], so that every warp has the same share of the costlier first kind),
+        //     in fp16: W rows -> rows 0..63 of the [W; Qe] operand; P W rows -> Qe = e^gamma q_hat - P W, rows
+        //     64..127; U rows -> U; P U rows -> O_intra
         {
             const int R = 32 * (warp & 3) + lane, cp = warp >> 2;
             const bool top = R < kBlock;
@@ -766,11 +717,9 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
                 const int c0 = 16 * (cp + 4 * cc);
                 float v[16];
                 tmem_ld16(tb + c0, v);
+                uint32_t off, step;
                 if (c0 < D) {
-                    if (top) {
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) v[c] = tf32_round(v[c]);
-                    } else {
+                    if (!top) {
                         float qh[16];
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
@@ -779,12 +728,16 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
                         }
                         const float e = egv[i];
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) v[c] = tf32_round(e * qh[c] - v[c]);
+                        for (int c = 0; c < 16; ++c) v[c] = e * qh[c] - v[c];
                     }
-                    put_afrag16(rec, R, c0, v, D, lane);
+                    off = rec16::wq(R, c0);
+                    step = 128;   // the next 8 columns: the core matrix adjacent along K
                 } else {
-                    put_cfrag16(rec + (top ? 192 : 256) * D, i, c0 - D, v, lane);
+                    off = (top ? rec16::kU : rec16::kO) + rec16::uo(i, c0 - D);
+                    step = 1024;  // the next 8 columns
                 }
+                *reinterpret_cast<uint4 *>(rec + off) = f8_to_h8(v);
+                *reinterpret_cast<uint4 *>(rec + off + step) = f8_to_h8(v + 8);
             }
         }
         tc_fence_before();

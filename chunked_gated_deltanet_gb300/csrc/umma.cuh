@@ -13,6 +13,7 @@
 // matrices adjacent along M/N (checked on the device for either major-ness).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <stdint.h>
 #include "mma.cuh"
 
@@ -40,6 +41,12 @@ __device__ __forceinline__ uint64_t umma_smem_desc(const void *p, uint32_t lbo, 
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, fp32 accumulator: kind::f16 with fp16 A and B (formats 0); a_mn / b_mn as above.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 
 // 2-D tensor copy of one box, global -> this CTA's shared memory, completing on an mbarrier.
@@ -79,7 +86,8 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
-// D[tmem] (+)= A * B for one K-step of 16 bf16, issued by one thread.
+// D[tmem] (+)= A * B for one K-step of 16 16-bit elements (bf16 or fp16, as the instruction descriptor says),
+// issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(
@@ -113,6 +121,26 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
+}
+
+// 8 fp16 (one 16-byte core-matrix row) -> fp32
+__device__ __forceinline__ void h8_to_f(uint4 u, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+// two fp32 -> an fp16 pair (round to nearest even), a in the low half
+__device__ __forceinline__ uint32_t f2_to_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+// 8 fp32 -> one 16-byte row of fp16
+__device__ __forceinline__ uint4 f8_to_h8(const float *v) {
+    return make_uint4(f2_to_h2(v[0], v[1]), f2_to_h2(v[2], v[3]), f2_to_h2(v[4], v[5]), f2_to_h2(v[6], v[7]));
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {

@@ -398,18 +398,20 @@ def test_checkpointing_prefill_equals_prefill_then_capture(cuda_device, dtype, d
         assert _same(s.S, r.S) and _same(sl.S, r.S) and _same(sl.conv, r.conv)
 
 
-def test_state_kernel_slice_width_does_not_change_results(cuda_device):
-    """A launch of more CTAs than SMs runs the state kernel with 32 columns per CTA instead of 16; the
-    arithmetic of every element is the same, so two sessions in one varlen call (256 CTAs at 16 columns:
-    the wide kernel) equal each session alone (128 CTAs: the narrow one) bit for bit."""
+@pytest.mark.parametrize("n_sess", [3, 5])
+def test_state_kernel_slice_width_does_not_change_results(cuda_device, n_sess):
+    """The state kernel takes d_v in slices of 32, 64 or 128 columns per CTA depending on how many chains a
+    launch holds (16 v-heads of d = 128: one session 32; three sessions 64; five 128). Every element's
+    arithmetic is the same in each width, so a varlen call of several sessions equals each session alone bit
+    for bit."""
     shape = wl.Shape(16, 16, 128, 128, 64, wl.BF16)
     runs = [Runner(shape, wl.Workload("width", shape, seed=70 + i, session_lengths=[300 + 190 * i]).session_tokens(0),
-                   wl.Workload("width", shape, seed=70).conv_weights(), cuda_device) for i in range(2)]
+                   wl.Workload("width", shape, seed=70).conv_weights(), cuda_device) for i in range(n_sess)]
     toks = [r.tok for r in runs]
     cu = np.cumsum([0] + [len(t) for t in toks]).tolist()
     x = wl.tokens_to_torch(wl.Tokens.concat(toks), shape.dtype, cuda_device)
-    ws = gdn.workspace(runs[0].desc, cu[-1] + 128, 2, cuda_device)
-    both = [runs[0].session(), runs[0].session()]
+    ws = gdn.workspace(runs[0].desc, cu[-1] + 64 * n_sess, n_sess, cuda_device)
+    both = [runs[0].session() for _ in range(n_sess)]
     out = torch.zeros((cu[-1], shape.n_v_heads, shape.d_v), device=cuda_device)
     gdn.gdn_prefill_varlen(runs[0].desc, both, cu, *x, runs[0].cw_t, out, ws, flags=gdn.GDN_ALLOW_PARTIAL)
     for i, r in enumerate(runs):

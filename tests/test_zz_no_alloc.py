@@ -85,15 +85,17 @@ def test_noalloc_matches_workspace_prefill_bit_for_bit(cuda_device):
 def test_noalloc_refuses_calls_beyond_its_scratch(cuda_device):
     shape = wl.Shape(16, 16, 128, 128, 512, wl.BF16)
     desc = gdn.make_desc(16, 16, 128, 128, 512)
-    need = gdn.gdn_workspace_size(desc, 1024, 1)
+    T = (_longest_call(desc) // 512 + 1) * 512   # the first whole-grid call beyond the built-in scratch
+    need = gdn.gdn_workspace_size(desc, T, 1)
     assert need > gdn.GDN_NOALLOC_SCRATCH_BYTES
     sess = gdn.Session(desc, cuda_device)
-    x = torch.zeros((1024, shape.channels), dtype=torch.bfloat16, device=cuda_device)
-    gb = torch.zeros((1024, 16), dtype=torch.float32, device=cuda_device)
-    out = torch.zeros((1024, 16, 128), dtype=torch.float32, device=cuda_device)
+    xqk = torch.zeros((T, 16 * 128), dtype=torch.bfloat16, device=cuda_device)
+    xv = torch.zeros((T, 16 * 128), dtype=torch.bfloat16, device=cuda_device)
+    gb = torch.zeros((T, 16), dtype=torch.float32, device=cuda_device)
+    out = torch.zeros((T, 16, 128), dtype=torch.float32, device=cuda_device)
     cw = torch.zeros((shape.channels, 4), dtype=torch.bfloat16, device=cuda_device)
     with pytest.raises(gdn.GdnError) as e:
-        gdn.gdn_prefill_chunks_noalloc(desc, sess, x, x, x, gb, gb, cw, out)
+        gdn.gdn_prefill_chunks_noalloc(desc, sess, xqk, xqk, xv, gb, gb, cw, out)
     assert e.value.status == gdn.GDN_ERR_WORKSPACE
     assert "built-in" in str(e.value)
     assert sess.committed == 0
