@@ -130,12 +130,13 @@ def test_noalloc_refusals_before_any_device_work(lib):
         return lib.gdn_prefill_chunks_noalloc(ctypes.byref(d), ctypes.byref(s), p, p, p, p, p, p, n_tokens, flags,
                                               p, ctypes.byref(nc), None)
 
-    need = gdn.gdn_workspace_size(d, 1024, 1)
+    T = 4096                      # whole grid chunks, far beyond the built-in scratch for this layer
+    need = gdn.gdn_workspace_size(d, T, 1)
     assert need > gdn.GDN_NOALLOC_SCRATCH_BYTES
-    assert call(1024) == gdn.GDN_ERR_WORKSPACE
+    assert call(T) == gdn.GDN_ERR_WORKSPACE
     assert b"built-in" in lib.gdn_last_error()
     assert call(-1) == gdn.GDN_ERR_INVALID_ARG
-    assert call(1024, flags=4) == gdn.GDN_ERR_INVALID_ARG
+    assert call(T, flags=4) == gdn.GDN_ERR_INVALID_ARG
     assert s.committed == 0 and nc.value == -7
 
 
