@@ -609,7 +609,7 @@ def other_config_measure(name: str, w, dev, steps: int, warmup: int = 3) -> dict
     if "prep_wy_tail" in rt and "prep_wy" in rt:
         a, b = rt.pop("prep_wy_tail"), rt["prep_wy"]
         rt["prep_wy"] = (a[0] + b[0], a[1] + b[1], a[2] + b[2])
-    prefill = {k: v for k, v in rt.items() if k in ("prep_wy", "state_output")}
+    prefill = {k: v for k, v in rt.items() if k in ("prep_wy", "state_output", "prefill_fused")}
     dom_name, (launches, timed, tot) = max(prefill.items(), key=lambda kv: kv[1][2])
     tokens_per_launch = step.tokens_per_step / (launches / steps)
     avg_ms = tot / max(timed, 1)

@@ -7,6 +7,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
+#include <random>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -99,7 +101,7 @@ namespace {
 // rounded up to 256 bytes (the kernels' widest stores want 32-byte alignment); `bytes` includes
 // that slack.
 struct WsLayout {
-    size_t qk_off, wu_off, bytes;
+    size_t qk_off, wu_off, flags_off, bytes;
 };
 constexpr size_t kWsAlign = 256;
 char *ws_base(void *workspace) {
@@ -112,11 +114,15 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 WsLayout ws_layout(const gdn_layer_desc *d, int64_t nblk) {
     WsLayout L;
     const int D = d->d_k;
+    L.flags_off = 0;
     if (d->in_dtype == GDN_BF16) {  // tensor-core path: one record per (block, v-head)
         L.qk_off = 0;
         L.wu_off = 0;
         const size_t rec = D == 128 ? gdn::rec16::kBytes : gdn::rec_floats(D) * sizeof(float);
-        L.bytes = kWsAlign + align256((size_t)nblk * d->n_v_heads * rec);
+        L.flags_off = align256((size_t)nblk * d->n_v_heads * rec);
+        // d = 128: a 64-bit publication flag per (block, q/k head) for the one-launch prefill
+        const size_t flags = D == 128 ? align256((size_t)nblk * d->n_qk_heads * sizeof(unsigned long long)) : 0;
+        L.bytes = kWsAlign + L.flags_off + flags;
         return L;
     }
     L.qk_off = 0;
@@ -124,6 +130,14 @@ WsLayout ws_layout(const gdn_layer_desc *d, int64_t nblk) {
     L.bytes = kWsAlign + L.wu_off + align256((size_t)nblk * d->n_v_heads * gdn::wu_floats(D) * sizeof(float));
     return L;
 }
+
+// Epochs of the one-launch prefill's publication flags: a fresh value per launch, starting from a random
+// 64-bit base, so that a flag left by an earlier call (or whatever a fresh workspace holds) does not read as
+// published except by a 2^-64 coincidence.
+std::atomic<unsigned long long> g_epoch{[] {
+    std::random_device rd;
+    return ((unsigned long long)rd() << 32) ^ (unsigned long long)rd() ^ 0x9e3779b97f4a7c15ULL;
+}()};
 
 // Bounded waits: default poll limit, and the test hook that makes the next launches' waits run out.
 constexpr long long kDefaultWaitLimit = 1LL << 24;
@@ -145,7 +159,7 @@ void fill_common(LaunchCommon &p, const gdn_layer_desc *d, const void *xq, const
 
 // 2-D tensor map over a row-major bf16 [rows][cols] input, boxes of 64 rows x 128 channels.
 // cuTensorMapEncodeTiled is reached through the runtime's driver entry point (no libcuda link).
-cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void *f = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -154,6 +168,11 @@ cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int6
             f = nullptr;
         return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
     }();
+    return fn;
+}
+
+cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+    const auto fn = tensor_map_encoder();
     if (!fn) return cudaErrorNotSupported;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)std::max<int64_t>(rows, 1)};
     const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
@@ -166,9 +185,10 @@ cudaError_t encode_rows_map(CUtensorMap *m, const void *base, int64_t rows, int6
 }
 
 // ---- optional per-kernel event timing ----
-enum Kind { K_PREP = 0, K_CONV = 1, K_STATE = 2, K_COPY = 3, K_DECODE = 4, K_GATES = 5, K_PREP_TAIL = 6, K_KINDS = 7 };
+enum Kind { K_PREP = 0, K_CONV = 1, K_STATE = 2, K_COPY = 3, K_DECODE = 4, K_GATES = 5, K_PREP_TAIL = 6, K_FUSED = 7,
+            K_KINDS = 8 };
 const char *const kKindName[K_KINDS] = {"prep_wy", "conv_commit", "state_output", "state_copy", "decode", "gates",
-                                        "prep_wy_tail"};
+                                        "prep_wy_tail", "prefill_fused"};
 
 struct Timing {
     bool on = false;
@@ -431,8 +451,19 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
             }
             cudaError_t e = gdn_device_error_word(&p.err);
             if (e != cudaSuccess) return cuda_fail(e, "device error word lookup");
-            const int split = in_bf16 && D == 128 ? tail_split(p, d) : 0;
-            if (split > 0) {
+            int sms = 0;
+            if ((e = gdn_sm_count(&sms)) != cudaSuccess) return cuda_fail(e, "SM count");
+            // few chains: the one-launch prefill (chains beside the prologue, at least half the SMs for it)
+            const int n_fused_chain = cnt * d->n_v_heads * (D / kFusedCols);
+            const bool fused = in_bf16 && D == 128 && 2 * n_fused_chain <= sms;
+            const int split = in_bf16 && D == 128 && !fused ? tail_split(p, d) : 0;
+            if (fused) {
+                p.task_block_major = 1;
+                auto *flags = reinterpret_cast<unsigned long long *>(ws_base(workspace) + L.flags_off);
+                const unsigned long long epoch = ++g_epoch;
+                e = launch_k(K_FUSED, cst, [&] { return gdn_launch_prefill_fused(p, ch, flags, epoch, n_fused_chain, cst); });
+                p.task_block_major = 0;
+            } else if (split > 0) {
                 // the call as two parts: blocks [0, split) (prologue, then state pass), then the prologue of
                 // the last blocks on the SMs that state pass leaves (running beside it), then their state
                 // pass, which continues from the first part's state
@@ -447,8 +478,6 @@ gdn_status prefill_impl(const gdn_layer_desc *d, gdn_session *sessions, int32_t 
                 rb.row0 += (int64_t)split * kBlock; rb.n -= split * kBlock; rb.blk0 += split;
                 rb.S0 = rb.S; rb.conv0 = rb.conv;   // the first part's results
                 pb.nblk = p.nblk - split;
-                int sms = 0;
-                if ((e = gdn_sm_count(&sms)) != cudaSuccess) return cuda_fail(e, "SM count");
                 const int cols = gdn_chain_umma_cols(d->n_v_heads, sms);
                 const int free_sms = sms - d->n_v_heads * (D / cols);
                 e = launch_k(K_PREP, cst, [&] { return gdn_launch_prep_umma(pa, ch, cst); });

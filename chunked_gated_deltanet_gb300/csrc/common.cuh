@@ -39,6 +39,7 @@ struct LaunchCommon {
     int nblk;                   // total blocks of this launch
     int blk_lo;                 // tcgen05 prologue: > 0 runs the tasks of blocks [blk_lo, nblk) only, beside the
                                 // state pass launched before it, and waits for that one at its end (see prep_umma.cu)
+    int task_block_major;       // tcgen05 prologue: tasks numbered block first (the one-launch prefill), else head first
     long long wait_limit;       // polls before a bounded mbarrier wait gives up
     unsigned int *err;          // device error word (bit 0: a bounded wait ran out)
     int debug_skip_first_copy;  // test hook: 1 = the state kernel, 2 = the tcgen05 prologue never issues its first copy
@@ -109,6 +110,18 @@ __device__ __forceinline__ int find_session(const LaunchCommon &p, int blk) {
     return s;
 }
 
+// Release / acquire of a 64-bit flag at GPU scope (the one-launch prefill's per-record flags).
+__device__ __forceinline__ void st_release_gpu(unsigned long long *a, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;\n" ::"l"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long *a) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(a) : "memory");
+    return v;
+}
+// Orders this thread's generic-proxy view of global memory with its async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;\n" ::: "memory"); }
+
 // Programmatic dependent launch: a kernel launched with programmatic stream serialization may start while
 // the kernel before it in the stream is still running. grid_dep_launch() lets the next kernel start (its
 // CTAs take SMs as ours leave); grid_dep_wait() returns once every earlier kernel has completed and its
@@ -167,6 +180,11 @@ cudaError_t gdn_launch_prep_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cu
 // max_ctas: at most that many CTAs (0: one per SM)
 cudaError_t gdn_launch_prep_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st, int max_ctas = 0);
 cudaError_t gdn_launch_chain_tc(const gdn::LaunchCommon &p, int D, int64_t ch, cudaStream_t st);
+// The one-launch prefill (bf16, d = 128): n_chain chain CTAs (64 d_v columns each) beside prologue CTAs on every
+// other SM; flags: [nblk][Hk] publication words in the workspace, epoch: this call's value for them.
+cudaError_t gdn_launch_prefill_fused(const gdn::LaunchCommon &p, int64_t ch, unsigned long long *flags,
+                                     unsigned long long epoch, int n_chain, cudaStream_t st);
+constexpr int kFusedCols = 64;   // d_v columns per chain CTA of the one-launch prefill
 // The tcgen05 state pass over fp16 records (d = 128); cols: d_v columns per CTA (32, 64 or 128; 0 chooses by the
 // launch's chain count, gdn_chain_umma_cols)
 cudaError_t gdn_launch_chain_umma(const gdn::LaunchCommon &p, int64_t ch, cudaStream_t st, int cols = 0);

@@ -80,7 +80,8 @@ struct UmmaCtl {
 };
 
 // A persistent CTA's tasks: blockIdx.x, + gridDim.x, ... of the launch's (nblk - blk_lo) x Hk tasks, task
-// tau = (block blk_lo + tau % (nblk - blk_lo), q/k head tau / (nblk - blk_lo)). A task source hands out task indices in the order the CTA runs
+// tau = (block blk_lo + tau % (nblk - blk_lo), q/k head tau / (nblk - blk_lo)) (or, with task_block_major,
+// (block blk_lo + tau / Hk, q/k head tau % Hk)). A task source hands out task indices in the order the CTA runs
 // them (first(), then next() until it returns -1, all CTA-uniform), tells which task next() will return
 // (peek(), -1 if none) and is told when a task's record is complete (done()).
 struct StridedTasks {
@@ -216,8 +217,13 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     struct Task { int blk, hk, pos0, n; int64_t row0; SessRef s; };
     auto task_of = [&](int tau) {
         Task k;
-        k.blk = p.blk_lo + tau % (p.nblk - p.blk_lo);
-        k.hk = tau / (p.nblk - p.blk_lo);
+        if (p.task_block_major) {
+            k.blk = p.blk_lo + tau / Hk;
+            k.hk = tau % Hk;
+        } else {
+            k.blk = p.blk_lo + tau % (p.nblk - p.blk_lo);
+            k.hk = tau / (p.nblk - p.blk_lo);
+        }
         k.s = p.s[find_session(p, k.blk)];
         k.pos0 = (k.blk - k.s.blk0) * kBlock;
         k.n = min(kBlock, k.s.n - k.pos0);
