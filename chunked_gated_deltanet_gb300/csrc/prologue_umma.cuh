@@ -10,11 +10,15 @@
 //   W = T diag(beta e^gamma) K_hat,  U = T diag(beta) V
 //   P_ij = e^{gamma_i - gamma_j} (Q K^T)_ij (j <= i)
 //   Qe = diag(e^gamma) Q_hat - P W,  O_intra = P U,  K_tilde = diag(e^{gamma_63 - gamma_j}) K_hat
-// and the record goes out in the fragment order the state kernel reads.
+// and the record goes out in fp16, in the operand layouts the state pass copies
+// straight into shared memory (common.cuh, rec16).
 //
-// The products run as tcgen05 MMAs of M = 128, issued by one thread, each
-// with bf16 hi/lo operand pairs (hi*hi + hi*lo + lo*hi, about 16 significant
-// bits per operand, fp32 accumulation). P W = (P T) Bk and P U = (P T) Bv, so
+// The products run as tcgen05 MMAs of M = 128, issued by one thread, with fp32
+// accumulation. [Q_hat; K_hat] K_hat^T takes bf16 hi/lo operand pairs (hi*hi +
+// hi*lo + lo*hi, about 16 significant bits per operand): the dot product of two
+// nearly orthogonal unit vectors cancels, and one rounding of the operands
+// would lose it. P T and the main product take single fp16 operands (11
+// significant bits, the precision of the record the state pass reads). P W = (P T) Bk and P U = (P T) Bv, so
 // stacking [T; P T] as the A operand gives all four 64 x 128 results of the
 // block in one product whose every accumulator row is used:
 //   [Q_hat; K_hat] K_hat^T               N = 64,  K = 128 -> TMEM columns 0..63 (kept for every v-head)
@@ -44,15 +48,15 @@ namespace up {   // shared-memory plan, bytes
 constexpr int D = 128;
 constexpr uint32_t AQ_LBO = 144, AQ_SBO = 16 * AQ_LBO;    // [q_hat; k_hat], K-major, K = 128, 16-byte gap between K cores
 constexpr uint32_t AQ_BYTES = 16 * AQ_SBO;                  // 128 rows
-constexpr uint32_t B_LBO = 128, B_SBO = 8 * B_LBO + 16;     // [beta e^gamma k_hat | beta v], MN-major, N = 256, K = 64
+constexpr uint32_t B_LBO = 128, B_SBO = 8 * B_LBO + 16;     // fp16 [beta e^gamma k_hat | beta v], MN-major, N = 256, K = 64
 constexpr uint32_t B_BYTES = 32 * B_SBO;
-constexpr uint32_t K64_LBO = 128, K64_SBO = 8 * K64_LBO;    // K = 64 operands: P, [T; P T] (K-major), T (MN-major)
+constexpr uint32_t K64_LBO = 128, K64_SBO = 8 * K64_LBO;    // K = 64 fp16 operands: P, [T; P T] (K-major), T (MN-major)
 constexpr uint32_t R64_BYTES = 8 * K64_SBO;                 // 64 rows (or 64 columns) of a K = 64 operand
 constexpr int LT = kBlock + 4;                              // fp32 A and T row pitch (floats)
 constexpr uint32_t OFF_AQH = 0, OFF_AQL = AQ_BYTES;
-constexpr uint32_t OFF_BH = 2 * AQ_BYTES, OFF_BL = OFF_BH + B_BYTES;
-constexpr uint32_t OFF_PH = OFF_BL + B_BYTES, OFF_PL = OFF_PH + R64_BYTES;     // P, K-major
-constexpr uint32_t OFF_TBH = OFF_PL + R64_BYTES, OFF_TBL = OFF_TBH + R64_BYTES; // T, MN-major (B of P T)
+constexpr uint32_t OFF_BH = 2 * AQ_BYTES, OFF_BL = OFF_BH + B_BYTES;            // B operand; OFF_BL: spare
+constexpr uint32_t OFF_PH = OFF_BL + B_BYTES, OFF_PL = OFF_PH + R64_BYTES;     // P, K-major; OFF_PL: spare
+constexpr uint32_t OFF_TBH = OFF_PL + R64_BYTES, OFF_TBL = OFF_TBH + R64_BYTES; // T, MN-major (B of P T); OFF_TBL: spare
 constexpr uint32_t OFF_AF = OFF_TBL + R64_BYTES;             // fp32 A (input of the inverse)
 constexpr uint32_t OFF_TF = OFF_AF + 4 * kBlock * LT;        // fp32 T
 constexpr uint32_t OFF_MT = OFF_TF + 4 * kBlock * LT;        // 2 x 16 x 24 inverse scratch
@@ -68,7 +72,7 @@ constexpr uint32_t OFF_RAW = OFF_PH;                         // raw input tiles:
 static_assert(OFF_RAW + 3 * RAW_TILE <= OFF_SMALL, "raw tiles must fit the P, T and inverse regions");
 static_assert(OFF_ATL + 2 * R64_BYTES <= OFF_MT, "[T; P T] must fit over A and T");
 static_assert(OFF_RAW % 128 == 0 && RAW_TILE % 128 == 0, "tensor-copy destinations 128-byte aligned");
-// the P T product reads 128 A rows from P's low half: the 64 rows after it are T's, in bounds
+// the P T product reads 128 A rows from P's region: the 64 rows after it (unused results) lie in the spare one
 static_assert(OFF_PL + 2 * R64_BYTES <= SMEM, "rows read past P's low part");
 static_assert(SMEM <= 227 * 1024, "shared memory");
 }  // namespace up
@@ -199,9 +203,8 @@ template <bool kAct, class Src>
 __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, unsigned char *sm, UmmaCtl *ctl,
                                              uint32_t tmem, Src &src) {
     using namespace up;
-    unsigned char *AQh = sm + OFF_AQH, *AQl = sm + OFF_AQL, *Bh = sm + OFF_BH, *Bl = sm + OFF_BL;
-    unsigned char *Ph = sm + OFF_PH, *Pl = sm + OFF_PL, *TBh = sm + OFF_TBH, *TBl = sm + OFF_TBL;
-    unsigned char *ATh = sm + OFF_ATH, *ATl = sm + OFF_ATL;
+    unsigned char *AQh = sm + OFF_AQH, *AQl = sm + OFF_AQL, *Bh = sm + OFF_BH;
+    unsigned char *Ph = sm + OFF_PH, *TBh = sm + OFF_TBH, *ATh = sm + OFF_ATH;
     float *Af = reinterpret_cast<float *>(sm + OFF_AF), *Tf = reinterpret_cast<float *>(sm + OFF_TF);
     float *Mt = reinterpret_cast<float *>(sm + OFF_MT);
     float *gam = reinterpret_cast<float *>(sm + OFF_SMALL), *bet = gam + kBlock, *egv = bet + kBlock;
@@ -317,6 +320,13 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         }
         umma_commit(&bar[1]);
     };
+    // single-pass fp16 MMA group D = A B over K, then a commit; thread 0 only
+    auto mma1 = [&](uint32_t d, uint64_t a, uint32_t astep, uint64_t b, uint32_t bstep, int K, uint32_t id) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int ks = 0; ks < K / 16; ++ks) umma_bf16(d, a + ((astep * ks) >> 4), b + ((bstep * ks) >> 4), id, ks > 0);
+        umma_commit(&bar[1]);
+    };
 
     // Row-parallel conv of rows [r0, r0 + nr) of a staged tile: lane owns channels 4 lane .. 4 lane + 3,
     // four rows at a time; outputs go through emit(i0, y[4][4]). The taps run on channel pairs in packed
@@ -373,12 +383,6 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         *reinterpret_cast<uint2 *>(hi + off) = make_uint2(h0, h1);
         *reinterpret_cast<uint2 *>(lo + off) = make_uint2(l0, l1);
     };
-    auto store8 = [&](unsigned char *hi, unsigned char *lo, uint32_t off, const float *v) {
-        uint4 h, l;
-        split8(v, h, l);
-        *reinterpret_cast<uint4 *>(hi + off) = h;
-        *reinterpret_cast<uint4 *>(lo + off) = l;
-    };
 
     // beta v of the staged v-head (row-parallel conv, groups of 4 rows) into channels 128..255 of the B operand:
     // every warp takes the 4-row group `warp` (all), or, while thread 0 issues the Q K^T product, warps 1-15
@@ -393,7 +397,8 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
                 float v[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) v[c] = i < n ? bet[i] * y[u][c] : 0.f;
-                split4_store(Bh, Bl, mnmajor_bf16_offset(128 + 4 * lane, i, B_LBO, B_SBO), v);
+                *reinterpret_cast<uint2 *>(Bh + mnmajor_bf16_offset(128 + 4 * lane, i, B_LBO, B_SBO)) =
+                    make_uint2(f2_to_h2(v[0], v[1]), f2_to_h2(v[2], v[3]));
             }
         };
 #pragma unroll 1
@@ -415,7 +420,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             const float sc = bet[j] * egv[j];
 #pragma unroll
             for (int c = 0; c < 8; ++c) v[c] *= sc;
-            store8(Bh, Bl, mnmajor_bf16_offset(8 * cg, j, B_LBO, B_SBO), v);
+            *reinterpret_cast<uint4 *>(Bh + mnmajor_bf16_offset(8 * cg, j, B_LBO, B_SBO)) = f8_to_h8(v);
         }
     };
 
@@ -567,8 +572,8 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
                 float pv[16];
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) pv[jj] = (j0 + jj) <= i ? v[jj] * dec[jj] : 0.f;
-                store8(Ph, Pl, kmajor_bf16_offset(i, j0, K64_LBO, K64_SBO), pv);
-                store8(Ph, Pl, kmajor_bf16_offset(i, j0 + 8, K64_LBO, K64_SBO), pv + 8);
+                *reinterpret_cast<uint4 *>(Ph + kmajor_bf16_offset(i, j0, K64_LBO, K64_SBO)) = f8_to_h8(pv);
+                *reinterpret_cast<uint4 *>(Ph + kmajor_bf16_offset(i, j0 + 8, K64_LBO, K64_SBO)) = f8_to_h8(pv + 8);
             } else {
                 const int i = R - kBlock;
                 float av[16];
@@ -657,8 +662,9 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             const float4 b = *reinterpret_cast<const float4 *>(Tf + i * LT + 8 * kg + 4);
             v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
             __syncthreads();   // every row of T is read before the first write over it
-            store8(ATh, ATl, kmajor_bf16_offset(i, 8 * kg, K64_LBO, K64_SBO), v);
-            store8(TBh, TBl, mnmajor_bf16_offset(8 * kg, i, K64_LBO, K64_SBO), v);
+            const uint4 th = f8_to_h8(v);
+            *reinterpret_cast<uint4 *>(ATh + kmajor_bf16_offset(i, 8 * kg, K64_LBO, K64_SBO)) = th;
+            *reinterpret_cast<uint4 *>(TBh + mnmajor_bf16_offset(8 * kg, i, K64_LBO, K64_SBO)) = th;
         }
         fence_proxy_async();
         tc_fence_before();
@@ -666,9 +672,8 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
 
         // 8. P T into TMEM columns 64..127; meanwhile the first half of the K_tilde^T record
         if (t == 0)
-            mma3(tmem + 64, umma_smem_desc(Ph, K64_LBO, K64_SBO), umma_smem_desc(Pl, K64_LBO, K64_SBO), 2 * K64_LBO,
-                 umma_smem_desc(TBh, K64_LBO, K64_SBO), umma_smem_desc(TBl, K64_LBO, K64_SBO), 2 * K64_LBO, kBlock,
-                 umma_idesc_bf16(128, 64, 0, 1));
+            mma1(tmem + 64, umma_smem_desc(Ph, K64_LBO, K64_SBO), 2 * K64_LBO, umma_smem_desc(TBh, K64_LBO, K64_SBO),
+                 2 * K64_LBO, kBlock, umma_idesc_f16(128, 64, 0, 1));
         mma_pending = 1;
         kt_record(0);   // the first half of K_tilde^T while the product runs, the second under the next one
         if (!(ok = wait_mma())) break;
@@ -678,8 +683,8 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             const int i = 32 * (warp & 3) + lane, c0 = 16 * (warp >> 2);
             float v[16];
             tmem_ld16(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 64 + c0, v);
-            store8(ATh, ATl, kmajor_bf16_offset(kBlock + i, c0, K64_LBO, K64_SBO), v);
-            store8(ATh, ATl, kmajor_bf16_offset(kBlock + i, c0 + 8, K64_LBO, K64_SBO), v + 8);
+            *reinterpret_cast<uint4 *>(ATh + kmajor_bf16_offset(kBlock + i, c0, K64_LBO, K64_SBO)) = f8_to_h8(v);
+            *reinterpret_cast<uint4 *>(ATh + kmajor_bf16_offset(kBlock + i, c0 + 8, K64_LBO, K64_SBO)) = f8_to_h8(v + 8);
         }
         fence_proxy_async();
         tc_fence_before();
@@ -687,9 +692,8 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
 
         // 10. [W U; P W P U] = [T; P T] [beta e^gamma k_hat | beta v] into TMEM columns 256..511
         if (t == 0)
-            mma3(tmem + 256, umma_smem_desc(ATh, K64_LBO, K64_SBO), umma_smem_desc(ATl, K64_LBO, K64_SBO), 2 * K64_LBO,
-                 umma_smem_desc(Bh, B_LBO, B_SBO), umma_smem_desc(Bl, B_LBO, B_SBO), 2 * B_LBO, kBlock,
-                 umma_idesc_bf16(128, 256, 0, 1));
+            mma1(tmem + 256, umma_smem_desc(ATh, K64_LBO, K64_SBO), 2 * K64_LBO, umma_smem_desc(Bh, B_LBO, B_SBO),
+                 2 * B_LBO, kBlock, umma_idesc_f16(128, 256, 0, 1));
         mma_pending = 1;
         kt_record(1);
         if (!(ok = wait_mma())) break;
