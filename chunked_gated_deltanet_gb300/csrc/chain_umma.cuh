@@ -60,6 +60,13 @@ constexpr int kChainWorkThreads = 256;   // warps 0-7 of a chain CTA
 constexpr int kCopier = 64;
 constexpr int kOwnCopier = kChainWorkThreads;
 
+// 8 fp32 values in one 32-byte store (dst 32-byte aligned): a whole sector per thread
+__device__ __forceinline__ void st_global_v8(float *dst, const float (&v)[8]) {
+    asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"l"(dst), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]),
+                 "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+                 : "memory");
+}
+
 // named barrier `id` over n threads (whole warps)
 __device__ __forceinline__ void uchain_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 // the same with an OR over the participants' predicates
@@ -277,6 +284,9 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
             const unsigned char *uo = stg + P::kOps + (q < 2 ? 0u : P::kUO) + (q < 2 ? row : i) * 16;
             const bool out_row = q >= 2 && i < s.n - b * kBlock;
             const int64_t o = ((s.row0 + (int64_t)b * kBlock + i) * p.Hv + h) * D + c0 + cl;
+            // 32-byte stores where the output allows them (every 8-column group of a row starts on a 32-byte
+            // boundary when the output does)
+            const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 #pragma unroll 1
             for (int j16 = 0; j16 < NC / 16; ++j16) {
                 float z[16];
@@ -308,6 +318,8 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
                             *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + o + 8 * j) =
                                 make_uint4(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&bb),
                                            *reinterpret_cast<const uint32_t *>(&c), *reinterpret_cast<const uint32_t *>(&d));
+                        } else if (out32) {
+                            st_global_v8(static_cast<float *>(p.out) + o + 8 * j, v);
                         } else {
                             float4 *of = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + o + 8 * j);
                             of[0] = make_float4(v[0], v[1], v[2], v[3]);

@@ -653,7 +653,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, cc, -1.f, lane);
         }
         __syncthreads();
-        //    T as bf16 hi/lo: rows 0..63 of [T; P T] (K-major, written over A and T) and the B operand of
+        //    T as fp16: rows 0..63 of [T; P T] (K-major, written over A and T) and the B operand of
         //    P T (MN-major)
         {
             const int i = t & 63, kg = t >> 6;
