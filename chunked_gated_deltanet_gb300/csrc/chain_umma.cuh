@@ -11,7 +11,8 @@
 //                                two accumulators that the epilogue adds (two issuers halve the issue time)
 //   U' = U - Z[0:64]             lanes 0..63 (warps 0, 1, 4, 5), rounded to fp16 into the B operand of dS
 //   O = Z[64:128] + O_intra      lanes 64..127 (warps 2, 3, 6, 7): the output rows, off the dependent path
-//   dS = K_tilde^T U'            128 x N: 4 MMAs, issued once the U' warps are done
+//   dS = K_tilde^T U'            128 x N: 4 MMAs (K_tilde^T read MN-major: the record keeps K_tilde by token
+//                                rows), issued once the U' warps are done
 //   S^T <- e^{gamma_63} S^T + dS warps 0-7, on the fp32 state rows they hold in registers (TMEM lane = d_k
 //                                row), written back as fp16 into the B operand of the next block's Z
 // The state enters a block's outputs and its delta-rule correction through W and Qe, and leaves it through
@@ -248,10 +249,11 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
     }
     const uint32_t tmem = *tslot;
     const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);   // this warp's lane quarter
-    constexpr uint32_t IDESC = umma_idesc_f16(128, N, 0, 1);
+    constexpr uint32_t IDESC = umma_idesc_f16(128, N, 0, 1);      // Z: A K-major, B MN-major
+    constexpr uint32_t IDESC_DS = umma_idesc_f16(128, N, 1, 1);   // dS: both MN-major
     const uint64_t dSB = umma_smem_desc(SB, 128, P::kSBO_S), dUB = umma_smem_desc(UB, 128, P::kSBO_U);
     // the stages' A operands: stage 1's descriptors are stage 0's plus the stage size (in 16-byte units)
-    const uint64_t dWQ0 = umma_smem_desc(sm + rec16::kWQ, 128, 2048), dKT0 = umma_smem_desc(sm + rec16::kKT, 128, 1024);
+    const uint64_t dWQ0 = umma_smem_desc(sm + rec16::kWQ, 128, 2048), dKT0 = umma_smem_desc(sm + rec16::kKT, 2048, 128);
     constexpr uint64_t kStageDesc = P::kStage >> 4;
 
     uint32_t pend = 0;   // threads 0 and 32: bit 0 a Z commit, bit 1 a dS commit, issued and not yet seen complete
@@ -335,7 +337,7 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
                     tc_fence_after();
                     const uint64_t a0 = dKT0 + (b & 1) * kStageDesc;
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + 2 * N, a0 + 16 * ks, dUB + 16 * ks, IDESC, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + 2 * N, a0 + 256 * ks, dUB + 16 * ks, IDESC_DS, ks > 0);
                     umma_commit(&bar[3]);
                     pend |= 2u;
                 }

@@ -85,8 +85,8 @@ __device__ __forceinline__ int cfrag_slice_index(int i, int c) {
 namespace rec16 {
 constexpr uint32_t kWQ = 0;         // [W; Qe], 128 x 128: A operand of [W; Qe] S^T, K-major cores, LBO 128 (along K),
                                     // SBO 2048 (along M)
-constexpr uint32_t kKT = 32768;     // K_tilde^T, 128 (d_k) x 64 (tokens): A operand of K_tilde^T U', K-major cores,
-                                    // LBO 128, SBO 1024
+constexpr uint32_t kKT = 32768;     // K_tilde^T, 128 (d_k) x 64 (tokens): A operand of K_tilde^T U', MN-major cores
+                                    // (a core row is 8 d_k channels of one token), LBO 2048 (along K), SBO 128 (along M)
 constexpr uint32_t kU = 49152;      // U, 64 x 128, as [column / 8][row][column % 8]: 1 KB per 8 columns
 constexpr uint32_t kO = 65536;      // O_intra, the same layout
 constexpr uint32_t kEg = 81920;     // e^{gamma_63} (fp32)
@@ -95,7 +95,7 @@ __host__ __device__ constexpr uint32_t wq(int r, int k) {
     return (uint32_t)(r >> 3) * 2048u + (uint32_t)(k >> 3) * 128u + (uint32_t)(r & 7) * 16u + (uint32_t)(k & 7) * 2u;
 }
 __host__ __device__ constexpr uint32_t kt(int d, int j) {
-    return kKT + (uint32_t)(d >> 3) * 1024u + (uint32_t)(j >> 3) * 128u + (uint32_t)(d & 7) * 16u + (uint32_t)(j & 7) * 2u;
+    return kKT + (uint32_t)(d >> 3) * 128u + (uint32_t)(j >> 3) * 2048u + (uint32_t)(j & 7) * 16u + (uint32_t)(d & 7) * 2u;
 }
 __host__ __device__ constexpr uint32_t uo(int i, int c) { return (uint32_t)(c >> 3) * 1024u + (uint32_t)i * 16u + (uint32_t)(c & 7) * 2u; }
 }  // namespace rec16

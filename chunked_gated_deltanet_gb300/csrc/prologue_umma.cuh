@@ -519,24 +519,23 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             if (!(ok = wait_in())) break;
         }
         unsigned char *rec = reinterpret_cast<unsigned char *>(p.ws_wu) + ((int64_t)blk * Hv + h) * rec16::kBytes;
-        // K_tilde^T as the fp16 K-major A operand (d_k x 64 tokens), half `part` of its 1,024 16-byte rows (row
-        // (d, tokens 8 jg .. 8 jg + 7)), by warps 1-15 (warp 0 issues the MMAs); e^{gamma_63} with the first half
+        // K_tilde^T as the fp16 MN-major A operand (d_k x 64 tokens): a 16-byte core row is 8 channels of one
+        // token's e^{gamma_63 - gamma_j} k_hat, so each comes from one row chunk of k_hat; half `part` of the
+        // 1,024 chunks, by warps 1-15 (warp 0 issues the MMAs), consecutive threads on consecutive record
+        // bytes; e^{gamma_63} with the first half
         auto kt_record = [&](int part) {
             if (warp == 0) return;
             constexpr int HALF = 512;
             const float gl = gam[kBlock - 1];
             for (int e = HALF * part + t - 32; e < HALF * (part + 1); e += kUmmaPrepThreads - 32) {
-                const int d = e & (D - 1), jg = e >> 7;
+                const int j = 8 * (e >> 7) + (e & 7), dg = (e >> 3) & 15;
+                const uint32_t o = kmajor_bf16_offset(kBlock + j, 8 * dg, AQ_LBO, AQ_SBO);
                 float v[8];
+                join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), v);
+                const float dec = __expf(gl - gam[j]);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int j = 8 * jg + jj;
-                    const uint32_t o = kmajor_bf16_offset(kBlock + j, d, AQ_LBO, AQ_SBO);
-                    const float kh = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQh + o)) +
-                                     __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(AQl + o));
-                    v[jj] = __expf(gl - gam[j]) * kh;
-                }
-                *reinterpret_cast<uint4 *>(rec + rec16::kt(d, 8 * jg)) = f8_to_h8(v);
+                for (int c = 0; c < 8; ++c) v[c] *= dec;
+                *reinterpret_cast<uint4 *>(rec + rec16::kt(8 * dg, j)) = f8_to_h8(v);
             }
             if (part == 0 && t == 32) *reinterpret_cast<float *>(rec + rec16::kEg) = expf(gl);
         };
