@@ -41,9 +41,13 @@ METRIC = "GDN prefill tokens/s per layer on 1 GB300 + % of tensor-pipe/HBM roofl
 UNIT = "tokens/s"
 # the arithmetic of the bf16-input path: what each stage computes in
 PRECISION = {"inputs": "bf16", "conv_norm_gates": "fp32",
-             "prologue_products": "tcgen05 kind::f16 on bf16 hi/lo operand pairs (hi*hi + hi*lo + lo*hi), fp32 accumulate",
+             "prologue_products": "tcgen05 kind::f16, fp32 accumulate: [q; k] k^T on bf16 hi/lo operand pairs "
+                                  "(hi*hi + hi*lo + lo*hi); P T and [T; P T] [beta e^gamma k | beta v] on single fp16 "
+                                  "operands",
              "triangular_inverse": "fp32 substitution + split-tf32 products",
-             "state_pass_products": "tf32 operands, fp32 accumulate", "state": "fp32", "outputs": "fp32"}
+             "record": "fp16 (W, Qe, K_tilde, U, O_intra) and fp32 e^gamma",
+             "state_pass_products": "tcgen05 kind::f16: fp16 operands (record, state copy, U'), fp32 accumulate",
+             "state": "fp32", "outputs": "fp32"}
 FALLBACK_HBM_GBS = 6800.0
 
 # Algorithmic HBM bytes per token of the fused layer: q and k per q/k head
@@ -839,9 +843,12 @@ def cpu_threads(n_heads: int) -> int:
 
 # kernel kind -> (the sources that define its code, its ncu summary); the summary's figures are used only
 # while the sha256 over those sources matches the one it records
-PROFILED = {"prep_wy": (("prep_umma.cu", "prologue_umma.cuh", "umma.cuh", "mma.cuh", "common.cuh"),
-                        "prep_umma_qwen08b_replay.md"),
-            "state_output": (("chain_tc.cu", "chain_tc.cuh", "mma.cuh", "common.cuh"), "state_output_qwen08b_replay.md")}
+PROFILED = {"prefill_fused": (("prefill_fused.cu", "chain_umma.cuh", "prologue_umma.cuh", "umma.cuh", "mma.cuh", "common.cuh"),
+                              "prefill_fused_qwen08b_replay.md"),
+            "prep_wy": (("prep_umma.cu", "prologue_umma.cuh", "umma.cuh", "mma.cuh", "common.cuh"),
+                        "prep_umma_long_session_branches.md"),
+            "state_output": (("chain_umma.cu", "chain_umma.cuh", "umma.cuh", "mma.cuh", "common.cuh"),
+                             "state_output_long_session_branches.md")}
 
 
 def source_sha16(names) -> str:
@@ -1000,7 +1007,7 @@ def main():
     # the state pass: tensor-pipe fraction against the tf32 rate measured now, and the single-session latency
     # floor (dependent 64-token block steps of one head x the measured time per step)
     state_pass = None
-    if "state_output" in ktimes:
+    if "state_output" in ktimes and "prefill_fused" not in ktimes:   # every call of the step in two launches
         launches, timed, tot = ktimes["state_output"]
         blocks = step.block_steps_per_step * args.steps
         us_block = tot * 1e3 / blocks
