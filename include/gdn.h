@@ -110,9 +110,11 @@ gdn_status gdn_session_init(const gdn_layer_desc *desc, gdn_session *session, fl
 
 /* Workspace bytes a prefill call needs for up to `max_tokens` tokens in total
  * over up to `max_sessions` sessions, for any 16-byte-aligned workspace pointer
- * (the size includes room for the library to align it further). Scratch of
- * one call: its contents are not needed afterwards, and calls that overlap on
- * the GPU must not share it. */
+ * (the size includes room for the library to align it further): the per-block
+ * records the prologue hands to the state pass and, for d = 128, the flags by
+ * which the one-launch prefill publishes them. Scratch of one call: its
+ * contents are not needed afterwards and need no clearing before, and calls
+ * that overlap on the GPU must not share it. */
 size_t gdn_workspace_size(const gdn_layer_desc *desc, int64_t max_tokens, int32_t max_sessions);
 
 /* Prefill of one session.
@@ -127,7 +129,12 @@ size_t gdn_workspace_size(const gdn_layer_desc *desc, int64_t max_tokens, int32_
  * chunk may be partial and the session may be left off grid: the next call on
  * it must be another partial call, a decode step or a restore.
  * Rows of `out` for consumed tokens are written; the others are untouched.
- * *n_consumed (host) receives the consumed count; session->committed grows by it. */
+ * *n_consumed (host) receives the consumed count; session->committed grows by it.
+ * Arithmetic: fp32 conv, norm, gates, triangular solve, accumulation and state;
+ * with bf16 inputs the block and state products take 16-bit operands (bf16
+ * hi/lo pairs for Q K^T, fp16 elsewhere, 11 significant bits), so conv outputs,
+ * U and state entries must stay within about 1e4 in magnitude (the fp16 range).
+ * fp32 inputs run fp32 throughout. */
 gdn_status gdn_prefill_chunks(const gdn_layer_desc *desc, gdn_session *session, const void *xq,
                               const void *xk, const void *xv, const float *g, const float *beta,
                               const void *conv_w, int64_t n_tokens, uint32_t flags, void *out,
@@ -198,7 +205,7 @@ gdn_status gdn_prefill_branches(const gdn_layer_desc *desc, const gdn_session *p
  * GDN_NOALLOC_SCRATCH_BYTES array inside the library, and the call allocates
  * nothing. A call whose processed tokens need more than that
  * (gdn_workspace_size(desc, tokens processed, 1) > GDN_NOALLOC_SCRATCH_BYTES;
- * about 700 tokens for 16 heads of d = 128) is refused with GDN_ERR_WORKSPACE
+ * 1,536 tokens for 16 heads of d = 128) is refused with GDN_ERR_WORKSPACE
  * before any device work. The first call on a device looks up the scratch's
  * device address (cudaGetSymbolAddress) with that device current: make that
  * first call before any stream capture. All calls in the process share the
