@@ -10,7 +10,7 @@ __global__ void __launch_bounds__(kChainWorkThreads, 1) chain_umma_kernel(const 
     grid_dep_launch();   // the next call's prologue may take SMs as this kernel's CTAs leave
     grid_dep_wait();     // the records of this call, the state and the conv state
     RecordsWritten ready;
-    chain_run<N, kChainWorkThreads>(p, ch, sm, blockIdx.x, ready);
+    chain_run<N, kChainWorkThreads, 8>(p, ch, sm, blockIdx.x, ready);
 }
 
 template <int N>

@@ -33,31 +33,34 @@
 
 namespace gdn {
 
-template <int N>
+template <int N, int NW = 8>
 struct UChainPlan {
     static_assert(N == 32 || N == 64 || N == 128, "columns per chain");
-    static constexpr int NC = N / 2;                         // columns per thread
+    static_assert(NW == 8 || NW == 16, "worker warps");
+    static constexpr int NC = N / (NW / 4);                  // columns per worker thread
     static constexpr uint32_t kOps = rec16::kU;              // [W; Qe] and K_tilde^T: the record's first 48 KB
     static constexpr uint32_t kUO = (uint32_t)N * 128;       // the chain's U (or O_intra) columns: N / 8 chunks of 1 KB
     static constexpr uint32_t kEgOff = kOps + 2 * kUO;       // e^{gamma_63} in a stage
     static constexpr uint32_t kTx = kEgOff + 16;             // bytes a stage receives per block
     static constexpr uint32_t kStage = (kTx + 1023) / 1024 * 1024;
-    static constexpr uint32_t kSB = 2 * kStage;              // fp16 S^T: B operand of Z, K = 128 (d_k) x N, MN-major
+    static constexpr int kS = 2;                             // record stages: the copies run kS - 1 blocks ahead
+    static constexpr uint32_t kSB = kS * kStage;             // fp16 S^T: B operand of Z, K = 128 (d_k) x N, MN-major
     static constexpr uint32_t kSBO_S = 2048;                 //   LBO 128 (along K), SBO 16 x 128 (along N)
     static constexpr uint32_t kUB = kSB + 128 * N * 2;       // fp16 U': B operand of dS, K = 64 (tokens) x N, MN-major
     static constexpr uint32_t kSBO_U = 1024;                 //   LBO 128, SBO 8 x 128
-    static constexpr uint32_t kBar = kUB + 64 * N * 2;       // mbarriers: [0, 1] stages, [2] Z (first half), [3] dS,
-                                                             // [4] Z (second half), [5, 6] stage released
-    static constexpr uint32_t kSlot = kBar + 7 * 8;          // TMEM allocation result
+    static constexpr uint32_t kBar = kUB + 64 * N * 2;       // mbarriers, indices below
+    static constexpr int kFull = 0, kZa = kS, kDS = kS + 1, kZb = kS + 2, kRel = kS + 3, kNBar = 2 * kS + 3;
+    // [kFull + i] stage i's copies landed, [kZa] / [kZb] the two halves of Z, [kDS] dS, [kRel + i] stage i released
+    static constexpr uint32_t kSlot = kBar + kNBar * 8;      // TMEM allocation result
     static constexpr uint32_t kBytes = kSlot + 16;
     static constexpr uint32_t kTmemCols = N == 32 ? 128 : (N == 64 ? 256 : 512);   // Z halves [0, 2N), dS [2N, 3N)
     static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
-constexpr int kChainWorkThreads = 256;   // warps 0-7 of a chain CTA
-// The thread that issues the record copies. In a CTA of 256 threads: lane 0 of warp 2 (output rows), one block
-// ahead, inside the step. In a larger CTA: lane 0 of warp 8, a warp of its own that polls the records'
-// publication and runs up to two blocks ahead, paced by the stage-released barriers.
+constexpr int kChainWorkThreads = 256;   // the standalone state kernel's CTA: 8 worker warps
+// The thread that issues the record copies, kS - 1 blocks ahead (kS record stages). When every warp of the CTA
+// is a worker: lane 0 of warp 2 (output rows), inside the step. With spare warps: lane 0 of warp 8, a warp of
+// its own that polls the records' publication, paced by the stage-released barriers.
 constexpr int kCopier = 64;
 constexpr int kOwnCopier = kChainWorkThreads;
 
@@ -147,15 +150,17 @@ __device__ __forceinline__ void chain_conv_commit(const LaunchCommon &p, int64_t
 }
 
 // Chain `cidx` (= ((rank * Hv) + v-head) * (128 / N) + slice, session p.order[rank]) on the CTA's shared memory
-// `sm` (UChainPlan<N>::kBytes bytes). Every thread of the CTA calls it (NT threads, 256 or more). ready(blk, hk)
+// `sm` (UChainPlan<N, NW>::kBytes bytes), with NW worker warps (8 or 16: warp w takes TMEM lane quarter w % 4 and
+// column group w / 4). Every thread of the CTA calls it (NT threads, NW * 32 or more). ready(blk, hk)
 // is called by the thread that issues the copies of launch block blk (q/k head hk) before it issues them; false
 // means it gave up waiting.
 // The dependent-launch wait is the caller's.
-template <int N, int NT, class Ready>
+template <int N, int NT, int NW, class Ready>
 __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, unsigned char *sm, int cidx, Ready &ready) {
-    static_assert(NT == kChainWorkThreads || NT >= kChainWorkThreads + 64, "threads");
-    constexpr bool kOwn = NT > kChainWorkThreads;   // a copier warp of its own, and conv-commit warps
-    using P = UChainPlan<N>;
+    constexpr int kWT = NW * 32;              // worker threads
+    static_assert(NT == kWT || (NW == 8 && NT >= kWT + 64), "threads");
+    constexpr bool kOwn = NT > kWT;           // a copier warp of its own, and conv-commit warps
+    using P = UChainPlan<N, NW>;
     constexpr int D = 128, NC = P::NC, nsl = D / N;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P::kBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P::kSlot);
@@ -165,14 +170,16 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
     const SessRef s = p.s[p.order[cidx / (nsl * p.Hv)]];
     const int c0 = sl * N;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31, q = warp & 3;
-    const bool worker = t < kChainWorkThreads;
+    const bool worker = t < kWT;
     const int row = 32 * q + lane;   // TMEM lane: the token row of Z (U' rows 0..63, output rows 64..127), the d_k row of dS
-    const int cl = ((warp >> 2) & 1) * NC;   // this thread's first column within the chain's N
+    const int cl = ((warp >> 2) & (NW / 4 - 1)) * NC;   // this thread's first column within the chain's N
     const int nb = (s.n + kBlock - 1) / kBlock;
     const unsigned char *recs = reinterpret_cast<const unsigned char *>(p.ws_wu);
 
+    constexpr int kS = P::kS;
+    const int copier = kOwn ? kOwnCopier : kCopier;
     if (t == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(&bar[i], 1);
+        for (int i = 0; i < P::kNBar; ++i) mbar_init(&bar[i], 1);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -181,12 +188,12 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
     }
     __syncthreads();   // barriers initialised (the first copies complete on them)
 
-    // block b's record part -> stage b & 1; false if the record never came
+    // block b's record part -> stage b % kS; false if the record never came
     auto issue = [&](int b) {
         if (!ready(s.blk0 + b, h / p.G)) return false;
-        unsigned char *stg = sm + (b & 1) * P::kStage;
+        unsigned char *stg = sm + (b % kS) * P::kStage;
         const unsigned char *r = recs + ((int64_t)(s.blk0 + b) * p.Hv + h) * rec16::kBytes;
-        uint64_t *br = &bar[b & 1];
+        uint64_t *br = &bar[P::kFull + b % kS];
         if (b == 0 && p.debug_skip_first_copy == 1) return true;   // test hook: leave the barrier pending
         fence_proxy_async();
         mbar_arrive_expect_tx(br, P::kTx);
@@ -198,7 +205,13 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
         return true;
     };
     __shared__ int s_ready0;   // block 0's record (and with it the session's first-block halo reads) is done
-    if (t == (kOwn ? kOwnCopier : 0)) s_ready0 = nb > 0 ? (int)issue(0) : 1;
+    int issued = -1;           // the copier: the last block whose copies it issued
+    if (t == copier) {         // the first kS - 1 blocks (a larger CTA's copier carries on in its own loop)
+        bool ok = true;
+        for (int b = 0; b < nb && b < (kOwn ? 1 : kS - 1) && ok; ++b)
+            if ((ok = issue(b))) issued = b;
+        s_ready0 = nb > 0 ? (int)(issued >= 0) : 1;
+    }
 
     // the state rows (d_k row `row`, this thread's columns) into registers, and their fp16 copy
     float st[NC];
@@ -224,27 +237,28 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
     tc_fence_after();
     int timed_out = s_ready0 ? 0 : 1;
     if (timed_out && t == 0) atomicOr(p.err, 1u);
-    // the conv state: by the warps after the copier's beside the block loop, else by every thread before it
-    // (the first block's record is published, so every halo read of the session's first block is done)
+    // the conv state (the first block's record is published, so every halo read of the session's first block is
+    // done): by the warps after the copier's beside the block loop; with 8 workers and no spare warps by every
+    // thread before the loop; with 16 workers after it
     if constexpr (kOwn) {
         if (warp > kOwnCopier / 32 && !timed_out) chain_conv_commit<N>(p, ch, s, h, sl, kOwnCopier + 32, NT - kOwnCopier - 32);
-    } else {
+    } else if constexpr (NW == 8) {
         if (!timed_out) chain_conv_commit<N>(p, ch, s, h, sl, 0, NT);
     }
-    // the copier warp: blocks 1, 2, ... in order, each once its stage is released (block b - 2 done) and its
+    // the copier warp: blocks 1, 2, ... in order, each once its stage is released (block b - kS done) and its
     // record published; afterwards it waits (bounded) until its last copies have landed
     if constexpr (kOwn) {
         if (t == kOwnCopier && !timed_out) {
-            int last = nb > 0 ? 0 : -1;
             bool ok = true;
             for (int b = 1; b < nb && ok; ++b) {
-                if (b >= 2 && !mbar_wait_bounded(&bar[5 + (b & 1)], ((b - 2) >> 1) & 1, p.wait_limit)) ok = false;
+                if (b >= kS && !mbar_wait_bounded(&bar[P::kRel + b % kS], ((b - kS) / kS) & 1, p.wait_limit)) ok = false;
                 if (ok && !issue(b)) ok = false;
-                if (ok) last = b;
+                if (ok) issued = b;
             }
             if (!ok) atomicOr(p.err, 1u);   // the block loop's waits then run out as well
-            for (int b = last > 0 ? last - 1 : 0; b <= last; ++b)
-                if (!(b == 0 && p.debug_skip_first_copy == 1)) mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
+            for (int b = issued - kS + 1 > 0 ? issued - kS + 1 : 0; b <= issued; ++b)
+                if (!(b == 0 && p.debug_skip_first_copy == 1))
+                    mbar_wait_bounded(&bar[P::kFull + b % kS], (b / kS) & 1, p.wait_limit);
         }
     }
     const uint32_t tmem = *tslot;
@@ -252,31 +266,35 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
     constexpr uint32_t IDESC = umma_idesc_f16(128, N, 0, 1);      // Z: A K-major, B MN-major
     constexpr uint32_t IDESC_DS = umma_idesc_f16(128, N, 1, 1);   // dS: both MN-major
     const uint64_t dSB = umma_smem_desc(SB, 128, P::kSBO_S), dUB = umma_smem_desc(UB, 128, P::kSBO_U);
-    // the stages' A operands: stage 1's descriptors are stage 0's plus the stage size (in 16-byte units)
+    // the stages' A operands: stage i's descriptors are stage 0's plus i stage sizes (in 16-byte units)
     const uint64_t dWQ0 = umma_smem_desc(sm + rec16::kWQ, 128, 2048), dKT0 = umma_smem_desc(sm + rec16::kKT, 2048, 128);
     constexpr uint64_t kStageDesc = P::kStage >> 4;
 
     uint32_t pend = 0;   // threads 0 and 32: bit 0 a Z commit, bit 1 a dS commit, issued and not yet seen complete
-    bool copy_next = false;   // kCopier: the copies of the block after the current one are in flight
+    bool copy_next = false;   // kCopier: the copies of block b + kS - 1 went out
     if (worker && !timed_out) {
         for (int b = 0; b < nb; ++b) {
-            const unsigned char *stg = sm + (b & 1) * P::kStage;
-            bool to = !mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);   // every worker reads the stage
+            const int si = b % kS;
+            const unsigned char *stg = sm + si * P::kStage;
+            bool to = !mbar_wait_bounded(&bar[P::kFull + si], (b / kS) & 1, p.wait_limit);   // every worker reads the stage
             if ((t == 0 || t == 32) && !to) {   // Z = [W; Qe] S^T, K = d_k: 4 steps of 16 per issuer (256 bytes each)
                 tc_fence_after();
                 const int k0 = t == 0 ? 0 : 4;
-                const uint64_t a0 = dWQ0 + (b & 1) * kStageDesc + 16 * k0, b0 = dSB + 16 * k0;
+                const uint64_t a0 = dWQ0 + si * kStageDesc + 16 * k0, b0 = dSB + 16 * k0;
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + (t == 0 ? 0 : N), a0 + 16 * ks, b0 + 16 * ks, IDESC, ks > 0);
-                umma_commit(&bar[t == 0 ? 2 : 4]);
+                umma_commit(&bar[t == 0 ? P::kZa : P::kZb]);
                 pend |= 1u;
             }
-            // the next block's copies, from an output-row warp (off the dependent path); the other stage was
-            // released at the end of step b - 1
-            if (!kOwn && t == kCopier) copy_next = b + 1 < nb && issue(b + 1);
+            // block b + kS - 1's copies, from an output-row warp (off the dependent path); its stage was released
+            // at the end of step b - 1
+            if (!kOwn && t == kCopier) {
+                copy_next = b + kS - 1 >= nb || issue(b + kS - 1);
+                if (copy_next && b + kS - 1 < nb) issued = b + kS - 1;
+            }
             {
-                const bool za = mbar_wait_bounded(&bar[2], b & 1, p.wait_limit);
-                const bool zb = mbar_wait_bounded(&bar[4], b & 1, p.wait_limit);
+                const bool za = mbar_wait_bounded(&bar[P::kZa], b & 1, p.wait_limit);
+                const bool zb = mbar_wait_bounded(&bar[P::kZb], b & 1, p.wait_limit);
                 if (!za || !zb) to = true;
                 if ((t == 0 && za) || (t == 32 && zb)) pend &= ~1u;
             }
@@ -332,17 +350,17 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
             }
             if (q < 2) {
                 fence_proxy_async();
-                uchain_bar(1, 128);   // warps 0, 1, 4, 5: U' complete
+                uchain_bar(1, kWT / 2);   // the U' warps (lane quarters 0 and 1): U' complete
                 if (t == 0 && !to) {  // dS = K_tilde^T U': K = 64 tokens in 4 steps
                     tc_fence_after();
-                    const uint64_t a0 = dKT0 + (b & 1) * kStageDesc;
+                    const uint64_t a0 = dKT0 + si * kStageDesc;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) umma_bf16(tmem + 2 * N, a0 + 256 * ks, dUB + 16 * ks, IDESC_DS, ks > 0);
-                    umma_commit(&bar[3]);
+                    umma_commit(&bar[P::kDS]);
                     pend |= 2u;
                 }
             }
-            if (!mbar_wait_bounded(&bar[3], b & 1, p.wait_limit)) to = true;
+            if (!mbar_wait_bounded(&bar[P::kDS], b & 1, p.wait_limit)) to = true;
             else if (t == 0) pend &= ~2u;
             tc_fence_after();
             {   // S^T <- e^{gamma_63} S^T + dS on this thread's rows, and the fp16 copy for the next block
@@ -357,11 +375,11 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
             tc_fence_before();
             // warps 0-7: state copy updated, Z and dS read, this stage free for block b + 2; uniform timeout
             // decision (a copy that was never issued counts as one)
-            if (uchain_bar_or(2, kChainWorkThreads, to || (!kOwn && t == kCopier && b + 1 < nb && !copy_next))) {
+            if (uchain_bar_or(2, kWT, to || (!kOwn && t == kCopier && !copy_next))) {
                 timed_out = b + 1;
                 break;
             }
-            if (kOwn && t == 0) mbar_arrive(&bar[5 + (b & 1)]);   // stage b & 1 released (for block b + 2)
+            if (kOwn && t == 0) mbar_arrive(&bar[P::kRel + si]);   // stage si released (for block b + kS)
             tc_fence_after();
         }
     }
@@ -370,14 +388,15 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
         const int b = timed_out - 1;
         if (t == 0) atomicOr(p.err, 1u);
         if (t == 0 || t == 32) {
-            if (pend & 1u) mbar_wait_bounded(&bar[t == 0 ? 2 : 4], b & 1, p.wait_limit);
-            if (pend & 2u) mbar_wait_bounded(&bar[3], b & 1, p.wait_limit);
+            if (pend & 1u) mbar_wait_bounded(&bar[t == 0 ? P::kZa : P::kZb], b & 1, p.wait_limit);
+            if (pend & 2u) mbar_wait_bounded(&bar[P::kDS], b & 1, p.wait_limit);
         }
-        if (!kOwn && t == kCopier && s_ready0 && nb > 0) {   // block b's copies (unless never issued) and block b + 1's
-            if (!(b == 0 && p.debug_skip_first_copy == 1)) mbar_wait_bounded(&bar[b & 1], (b >> 1) & 1, p.wait_limit);
-            if (copy_next) mbar_wait_bounded(&bar[(b + 1) & 1], ((b + 1) >> 1) & 1, p.wait_limit);
-        }
+        if (!kOwn && t == kCopier)   // blocks b .. issued (unless the test hook held block 0 back)
+            for (int j = b; j <= issued; ++j)
+                if (!(j == 0 && p.debug_skip_first_copy == 1))
+                    mbar_wait_bounded(&bar[P::kFull + j % kS], (j / kS) & 1, p.wait_limit);
     } else if (worker) {   // the final state (and its checkpoint)
+        if constexpr (!kOwn && NW == 16) chain_conv_commit<N>(p, ch, s, h, sl, 0, kWT);
         float *Sg = s.S + ((int64_t)h * D + row) * D + c0 + cl;
         float *Sc = s.S_cap ? s.S_cap + ((int64_t)h * D + row) * D + c0 + cl : nullptr;
 #pragma unroll

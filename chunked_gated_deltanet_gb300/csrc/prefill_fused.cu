@@ -1,6 +1,8 @@
 // The one-launch prefill (bf16 inputs, d = 128) for calls with few chains: one persistent CTA per SM.
 //
-// CTAs [0, n_chain) run the state pass, one chain each (session, v-head, 64 columns of d_v; chain_umma.cuh).
+// CTAs [0, n_chain) run the state pass, one chain each (session, v-head, 64 columns of d_v; chain_umma.cuh), on
+// 8 worker warps; warp 8 polls the records' publication and issues the copies, warps 9-15 commit the conv state.
+// (All 16 warps as workers, with the polls inside the step, measured slower.)
 // The other CTAs run the prologue (prologue_umma.cuh) over the call's (64-token block, q/k head) tasks in
 // block order, CTA j taking tasks j, j + P, j + 2P, ... of the P prologue CTAs. A task's record, once
 // written, is published by a release store of this call's epoch into its flag; the chain CTA that needs it
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     grid_dep_wait();     // the states, conv states and workspace of earlier work
     if ((int)blockIdx.x < f.n_chain) {
         FlagReady ready{f.flags, f.epoch, p.Hk, p.wait_limit};
-        chain_run<kFusedCols, kUmmaPrepThreads>(p, ch, sm, blockIdx.x, ready);
+        chain_run<kFusedCols, kUmmaPrepThreads, 8>(p, ch, sm, blockIdx.x, ready);
         return;
     }
     UmmaCtl *ctl = reinterpret_cast<UmmaCtl *>(sm + up::OFF_BAR);
@@ -96,7 +98,8 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
 cudaError_t gdn_launch_prefill_fused(const gdn::LaunchCommon &p, int64_t ch, unsigned long long *flags,
                                      unsigned long long epoch, int n_chain, cudaStream_t st) {
     using namespace gdn;
-    constexpr size_t smem = up::SMEM > UChainPlan<kFusedCols>::kBytes ? up::SMEM : UChainPlan<kFusedCols>::kBytes;
+    constexpr size_t chain_smem = UChainPlan<kFusedCols, 8>::kBytes;
+    constexpr size_t smem = up::SMEM > chain_smem ? up::SMEM : chain_smem;
     static_assert(smem <= 227 * 1024, "shared memory");
     auto k = p.act ? prefill_fused_kernel<true> : prefill_fused_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
