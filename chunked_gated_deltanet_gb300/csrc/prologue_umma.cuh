@@ -31,8 +31,8 @@
 // CUDA cores for its 16 x 16 diagonal blocks, split-tf32 mma.sync for the
 // blocked products. The input tiles arrive as 2-D tensor copies (one per tile)
 // plus three single-row halo copies, on an mbarrier: a task's tiles are
-// prefetched into L2 at the start of the task before it and copied in during
-// that task's record epilogue. Every wait is bounded, and on a timeout the CTA
+// copied in during the inverse of the task before it (their region is their
+// own), by warps that are idle there. Every wait is bounded, and on a timeout the CTA
 // records it in the device error word, waits (bounded) for what it has in
 // flight and returns (the kernel then frees its TMEM).
 #pragma once
@@ -54,28 +54,38 @@ constexpr uint32_t K64_LBO = 128, K64_SBO = 8 * K64_LBO;    // K = 64 fp16 opera
 constexpr uint32_t R64_BYTES = 8 * K64_SBO;                 // 64 rows (or 64 columns) of a K = 64 operand
 constexpr int LT = kBlock + 4;                              // fp32 A and T row pitch (floats)
 constexpr uint32_t OFF_AQH = 0, OFF_AQL = AQ_BYTES;
-constexpr uint32_t OFF_BH = 2 * AQ_BYTES, OFF_BL = OFF_BH + B_BYTES;            // B operand; OFF_BL: spare
-constexpr uint32_t OFF_PH = OFF_BL + B_BYTES, OFF_PL = OFF_PH + R64_BYTES;     // P, K-major; OFF_PL: spare
-constexpr uint32_t OFF_TBH = OFF_PL + R64_BYTES, OFF_TBL = OFF_TBH + R64_BYTES; // T, MN-major (B of P T); OFF_TBL: spare
-constexpr uint32_t OFF_AF = OFF_TBL + R64_BYTES;             // fp32 A (input of the inverse)
+constexpr uint32_t OFF_BH = 2 * AQ_BYTES;                    // B operand
+constexpr uint32_t OFF_PH = OFF_BH + B_BYTES;                // P, K-major
+constexpr uint32_t OFF_TBH = OFF_PH + R64_BYTES;             // T, MN-major (B of P T)
+constexpr uint32_t OFF_AF = OFF_TBH + R64_BYTES;             // fp32 A (input of the inverse)
 constexpr uint32_t OFF_TF = OFF_AF + 4 * kBlock * LT;        // fp32 T
 constexpr uint32_t OFF_MT = OFF_TF + 4 * kBlock * LT;        // 2 x 16 x 24 inverse scratch
-constexpr uint32_t OFF_ATH = OFF_AF, OFF_ATL = OFF_ATH + 2 * R64_BYTES;   // [T; P T], K-major, over A and T
+constexpr uint32_t OFF_ATH = OFF_AF;                         // [T; P T], K-major, over A and T
 constexpr uint32_t OFF_SMALL = OFF_MT + 4 * 2 * 16 * 24;     // gamma, beta, e^gamma
 constexpr uint32_t W_BYTES = D * 4 * 2;                      // conv weights of one head's channels (bf16 [D][4])
 constexpr uint32_t OFF_W = OFF_SMALL + 4 * 3 * kBlock;       // q, k, v conv weights
-constexpr uint32_t OFF_BAR = OFF_W + 3 * W_BYTES;            // the control words (UmmaCtl) of the standalone kernel
-constexpr uint32_t SMEM = OFF_BAR + 32;                      // the operand plan ends at OFF_BAR
 constexpr uint32_t RAW_ROW = 2 * D, RAW_TILE = (kBlock + 3) * RAW_ROW;
-constexpr uint32_t TILE_BYTES = RAW_TILE + W_BYTES;           // one staged tile: 64 + 3 rows and its weights
-constexpr uint32_t OFF_RAW = OFF_PH;                         // raw input tiles: dead before P, T, A are written
-static_assert(OFF_RAW + 3 * RAW_TILE <= OFF_SMALL, "raw tiles must fit the P, T and inverse regions");
-static_assert(OFF_ATL + 2 * R64_BYTES <= OFF_MT, "[T; P T] must fit over A and T");
+constexpr uint32_t TILE_BYTES = RAW_TILE + W_BYTES;          // one staged tile: 64 + 3 rows and its weights
+constexpr uint32_t OFF_RAW = OFF_W + 3 * W_BYTES;            // raw input tiles, a region of their own: the next
+                                                             // task's copies land while this one still computes
+constexpr uint32_t OFF_BAR = OFF_RAW + 3 * RAW_TILE;         // the control words (UmmaCtl) of the standalone kernel
+constexpr uint32_t OFF_SESS = OFF_BAR + 32;                  // the launch's sessions (SessLite), read per task
+constexpr uint32_t OFF_NEXT = OFF_SESS + 24 * kLaunchSessions;   // the next task, for every thread
+constexpr uint32_t SMEM = OFF_NEXT + 64;
+static_assert(OFF_ATH + 2 * R64_BYTES <= OFF_MT, "[T; P T] must fit over A and T");
 static_assert(OFF_RAW % 128 == 0 && RAW_TILE % 128 == 0, "tensor-copy destinations 128-byte aligned");
-// the P T product reads 128 A rows from P's region: the 64 rows after it (unused results) lie in the spare one
-static_assert(OFF_PL + 2 * R64_BYTES <= SMEM, "rows read past P's low part");
+// the P T product reads 128 A rows from P's region: the 64 rows after it (unused results) are T's operand
+static_assert(OFF_PH + 2 * R64_BYTES <= OFF_AF, "rows read past P");
 static_assert(SMEM <= 227 * 1024, "shared memory");
 }  // namespace up
+
+// What a task needs of its session, copied into shared memory once per CTA.
+struct SessLite {
+    int64_t row0;         // first row of the session's tokens
+    const void *conv0;    // the conv state it starts from
+    int32_t n, blk0;      // tokens of this call, first block
+};
+static_assert(sizeof(SessLite) == 24, "session entry");
 
 // Control words of the prologue, kept apart from its operand plan.
 struct UmmaCtl {
@@ -214,29 +224,51 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     __nv_bfloat16 *wq = reinterpret_cast<__nv_bfloat16 *>(sm + OFF_W), *wk = wq + 4 * D, *wv = wk + 4 * D;
 
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int Hk = p.Hk, Hv = p.Hv;
+    // the launch parameters used inside the task loop, read once (each later read of a field is a load)
+    const int Hk = p.Hk, Hv = p.Hv, G = p.G, blk_lo = p.blk_lo, nblk = p.nblk;
+    const bool block_major = p.task_block_major != 0;
+    const int n_sess = p.n_sess;
+    const long long wait_limit = p.wait_limit;
+    const float *gate_g = p.g, *gate_beta = p.beta;
     const int64_t nq = (int64_t)Hk * D, nv = (int64_t)Hv * D;
     const __nv_bfloat16 *cw = static_cast<const __nv_bfloat16 *>(p.conv_w);
-    struct Task { int blk, hk, pos0, n; int64_t row0; SessRef s; };
+    struct Task { int blk, hk, pos0, n; int64_t row0, srow0; const void *conv0; };
+    // the session of block blk: the last one that starts at or before it (a binary search in shared memory)
+    const SessLite *sess = reinterpret_cast<const SessLite *>(sm + OFF_SESS);
     auto task_of = [&](int tau) {
         Task k;
-        if (p.task_block_major) {
-            k.blk = p.blk_lo + tau / Hk;
+        if (block_major) {
+            k.blk = blk_lo + tau / Hk;
             k.hk = tau % Hk;
         } else {
-            k.blk = p.blk_lo + tau % (p.nblk - p.blk_lo);
-            k.hk = tau / (p.nblk - p.blk_lo);
+            k.blk = blk_lo + tau % (nblk - blk_lo);
+            k.hk = tau / (nblk - blk_lo);
         }
-        k.s = p.s[find_session(p, k.blk)];
-        k.pos0 = (k.blk - k.s.blk0) * kBlock;
-        k.n = min(kBlock, k.s.n - k.pos0);
-        k.row0 = k.s.row0 + k.pos0;
+        int lo = 0;
+        for (int hi = n_sess - 1; lo < hi;) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sess[mid].blk0 <= k.blk) lo = mid;
+            else hi = mid - 1;
+        }
+        const SessLite ss = sess[lo];
+        k.pos0 = (k.blk - ss.blk0) * kBlock;
+        k.n = min(kBlock, ss.n - k.pos0);
+        k.row0 = ss.row0 + k.pos0;
+        k.srow0 = ss.row0;
+        k.conv0 = ss.conv0;
         return k;
     };
     if (t == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         mbar_init_fence();
+    }
+    if (t < n_sess) {
+        SessLite *w = reinterpret_cast<SessLite *>(sm + OFF_SESS) + t;
+        w->row0 = p.s[t].row0;
+        w->conv0 = p.s[t].conv0;
+        w->n = p.s[t].n;
+        w->blk0 = p.s[t].blk0;
     }
     __syncthreads();
     int tau = src.first();
@@ -245,16 +277,17 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         __syncthreads();
         return true;
     }
-    Task cur = task_of(tau), nxt = cur;
+    Task cur = task_of(tau);
     int blk = cur.blk, hk = cur.hk, n = cur.n, ntau = -1;
     uint32_t in_phase = 0, mma_phase = 0;
     int in_pending = 0, mma_pending = 0;   // an issued copy group / MMA group not yet seen complete (CTA-uniform)
 
     // Stage rows pos0-3 .. pos0+63 of task k's q and k tiles (with_qk) and of v-head h's v tile, with their
     // conv weights: one tensor copy of the block's 64 rows per tile (rows past the inputs read as zero, rows
-    // past n belong to other tokens and only reach masked results), issued by thread 0 with the byte count;
+    // past n belong to other tokens and only reach masked results), issued by thread 256 with the byte count;
     // the three halo rows (from the inputs or, before a call's first token, from the conv state) and the
-    // weights as single bulk copies, one per warp 1.., so that no warp waits on them.
+    // weights as single bulk copies, one per issuing thread (lanes 0 and 1 of warps 8-15). Every thread calls
+    // it; the issuing threads are those that are idle while the inverse runs, where the next copies go out.
     struct Tile { __nv_bfloat16 *dst, *wdst; const CUtensorMap *map; const __nv_bfloat16 *x; int64_t ld, col0, chan0; };
     auto tile_of = [&](int q, const Task &k, int h) -> Tile {
         if (q == 0) return {rawq, wq, &p.tm_q, static_cast<const __nv_bfloat16 *>(p.xq), nq, (int64_t)k.hk * D, (int64_t)k.hk * D};
@@ -263,26 +296,26 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         return {rawv, wv, &p.tm_v, static_cast<const __nv_bfloat16 *>(p.xv), nv, (int64_t)h * D, 2 * nq + (int64_t)h * D};
     };
     auto stage = [&](const Task &k, int h, bool with_qk, bool skip) {
-        in_pending = 1;
         if (skip) return;
         const int q0 = with_qk ? 0 : 2, ntile = 3 - q0;
-        // the region was last written by generic stores (ordered by the barriers since): order them
-        // before the async-proxy writes of the copies
-        if (t == 0 || (lane == 0 && warp >= 1 && warp <= 4 * ntile)) fence_proxy_async();
-        if (t == 0) {
+        const int e = t >= 256 && lane < 2 ? ((t - 256) >> 5) + 8 * lane : 64;   // this thread's halo row or weights
+        // the region was last read by generic loads (ordered by the barriers since): order them before the
+        // async-proxy writes of the copies
+        if (t == 256 || e < 4 * ntile) fence_proxy_async();
+        if (t == 256) {
             mbar_arrive_expect_tx(&bar[0], (uint32_t)ntile * TILE_BYTES);
             for (int q = q0; q < 3; ++q) {
                 const Tile tl = tile_of(q, k, h);
                 tma_load_2d(tl.dst + 3 * D, tl.map, (int)tl.col0, (int)k.row0, &bar[0]);
             }
         }
-        if (lane == 0 && warp >= 1 && warp <= 4 * ntile) {
-            const int e = warp - 1, r = e & 3;
+        if (e < 4 * ntile) {
+            const int r = e & 3;
             const Tile tl = tile_of(q0 + (e >> 2), k, h);
             if (r < 3) {
                 const int pos = k.pos0 - 3 + r;
-                const __nv_bfloat16 *src = pos < 0 ? static_cast<const __nv_bfloat16 *>(k.s.conv0) + (int64_t)(3 + pos) * ch + tl.chan0
-                                                   : tl.x + (k.s.row0 + pos) * tl.ld + tl.col0;
+                const __nv_bfloat16 *src = pos < 0 ? static_cast<const __nv_bfloat16 *>(k.conv0) + (int64_t)(3 + pos) * ch + tl.chan0
+                                                   : tl.x + (k.srow0 + pos) * tl.ld + tl.col0;
                 bulk_g2s(tl.dst + r * D, src, RAW_ROW, &bar[0]);
             } else {
                 bulk_g2s(tl.wdst, cw + tl.chan0 * 4, W_BYTES, &bar[0]);
@@ -291,14 +324,14 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     };
     // every thread waits; true when the phase completed for all of them (CTA-uniform)
     auto wait_in = [&]() {
-        const bool ok = mbar_wait_bounded(&bar[0], in_phase, p.wait_limit);
+        const bool ok = mbar_wait_bounded(&bar[0], in_phase, wait_limit);
         if (__syncthreads_or(!ok)) return false;
         in_phase ^= 1u;
         in_pending = 0;
         return true;
     };
     auto wait_mma = [&]() {
-        const bool ok = mbar_wait_bounded(&bar[1], mma_phase, p.wait_limit);
+        const bool ok = mbar_wait_bounded(&bar[1], mma_phase, wait_limit);
         if (__syncthreads_or(!ok)) return false;
         mma_phase ^= 1u;
         mma_pending = 0;
@@ -424,20 +457,21 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         }
     };
 
-    stage(cur, hk * p.G, true, p.debug_skip_first_copy == 2);   // 1. the first task's tiles
-    // gamma (inclusive scan of g over the block), beta and e^gamma of v-head h, by warps 2 and 3 alone: warp 3
-    // adds the total of rows 0..31 itself, so no barrier is needed. The loads can be issued early (for the
-    // next task, during the current one's record epilogue) and the scan run later.
-    const int jg = t - 64;
+    stage(cur, hk * G, true, p.debug_skip_first_copy == 2);   // 1. the first task's tiles
+    in_pending = 1;
+    // gamma (inclusive scan of g over the block), beta and e^gamma of v-head h, by warps 8 and 9 alone: warp 9
+    // adds the total of rows 0..31 itself, so no barrier is needed. The loads are issued early (for the
+    // next head or task, while the inverse of the current one runs) and the scan run later.
+    const int jg = t - 256;
     struct Gv { float g, b, lo; };
     auto gates_load = [&](const Task &k, int h) {
         Gv r{0.f, 0.f, 0.f};
         if (jg < 0 || jg >= kBlock) return r;
         if (jg < k.n) {
-            r.g = p.g[(k.row0 + jg) * Hv + h];
-            r.b = p.beta[(k.row0 + jg) * Hv + h];
+            r.g = gate_g[(k.row0 + jg) * Hv + h];
+            r.b = gate_beta[(k.row0 + jg) * Hv + h];
         }
-        if (jg >= 32 && lane < k.n) r.lo = p.g[(k.row0 + lane) * Hv + h];
+        if (jg >= 32 && lane < k.n) r.lo = gate_g[(k.row0 + lane) * Hv + h];
         return r;
     };
     auto gates_store = [&](Gv r) {
@@ -457,21 +491,11 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         bet[jg] = r.b;
         egv[jg] = expf(sv);
     };
-    gates_store(gates_load(cur, hk * p.G));
+    gates_store(gates_load(cur, hk * G));
     Gv gnext{0.f, 0.f, 0.f}, ghead{0.f, 0.f, 0.f};
     bool ok = true;
     for (;;) {   // tasks
     ok = wait_in();
-    if (ok && t == 32) {   // the next task's input tiles and gates into L2, a task ahead of their loads
-        const int pt = src.peek();
-        if (pt >= 0) {
-            const Task k = task_of(pt);
-            tma_prefetch_2d(&p.tm_q, k.hk * D, (int)k.row0);
-            tma_prefetch_2d(&p.tm_k, k.hk * D, (int)k.row0);
-            for (int gi = 0; gi < p.G; ++gi) tma_prefetch_2d(&p.tm_v, (k.hk * p.G + gi) * D, (int)k.row0);
-            prefetch_gates(p, k.row0, k.n);
-        }
-    }
 
     if (ok) {
         // 2. conv + L2 norm of q (warps 0-7) and k (warps 8-15), 8 rows per warp -> bf16 hi/lo rows of [q_hat; k_hat]
@@ -512,8 +536,8 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     }
 
     // 4. each v-head of the group
-    for (int gi = 0; ok && gi < p.G; ++gi) {
-        const int h = hk * p.G + gi;
+    for (int gi = 0; ok && gi < G; ++gi) {
+        const int h = hk * G + gi;
         if (gi > 0) {   // this head's v tile was staged during the previous head's record epilogue
             gates_store(ghead);
             if (!(ok = wait_in())) break;
@@ -586,10 +610,19 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         tc_fence_before();
         __syncthreads();
 
+        // the next v-head's v tile, or the next task's inputs: every raw tile and weight of this head has been
+        // read, so their region takes the next copies now, a whole head's work ahead of their use. Warps 8-15,
+        // idle in the inverse, work out the next task (and leave it in shared memory for the other warps),
+        // issue the copies and load the gates (which go to shared memory once this head's record is written).
+        const bool next_head = gi + 1 < G;
+        const int ptau = next_head ? -1 : src.peek();   // the task that next() returns at the end of this one
+        const bool stage_next = next_head || ptau >= 0;
+        if (stage_next) in_pending = 1;
+
         // 7. T = (I + A)^{-1} (unit lower triangular) in fp32, two levels of 2x2 blocking, products as
         //    split-tf32 MMAs, one 16 x 8 tile per warp:
         //    (a) diagonal 16x16 blocks D_b by substitution, one column per thread (warp 0: D_0, D_1; warp 1:
-        //        D_2, D_3); warps 8-15 zero the blocks above the diagonal meanwhile;
+        //        D_2, D_3); warps 8-15 zero the blocks above the diagonal, then issue the copies above;
         //    (b) warps 0-3 (block pair (b + 1, b), column tile nt): T_10 = -D_1 (A_10 D_0), T_32 = -D_3 (A_32 D_2);
         //    (c) warps 0-7 (row tile mt, column tile nt): X = A[32:64, 0:32] T[0:32, 0:32], then
         //        T[32:64, 0:32] = -T[32:64, 32:64] X.
@@ -620,6 +653,15 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
                 const int bi = e >> 6, r = (e >> 2) & 15, c4 = e & 3;
                 const int ib = bi < 3 ? 0 : (bi < 5 ? 1 : 2), jb = bi < 3 ? bi + 1 : (bi < 5 ? bi - 1 : 3);
                 *reinterpret_cast<float4 *>(Tf + (16 * ib + r) * LT + 16 * jb + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (stage_next) {
+                const Task k = next_head ? cur : task_of(ptau);
+                const int hs = next_head ? h + 1 : k.hk * G;
+                if (!next_head && t == 256) *reinterpret_cast<Task *>(sm + OFF_NEXT) = k;
+                stage(k, hs, !next_head, false);
+                const Gv gv = gates_load(k, hs);
+                if (next_head) ghead = gv;
+                else gnext = gv;
             }
         }
         if (warp < 4) {   // (b)
@@ -697,21 +739,6 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         kt_record(1);
         if (!(ok = wait_mma())) break;
 
-        // the next v-head's v tile, or the next task's inputs: the raw-tile region and the weights are free
-        // from here on (the gates go to shared memory once this head's record is written)
-        // (one call site for both, so that the staging code appears once)
-        {
-            const bool next_head = gi + 1 < p.G;
-            if (!next_head && (ntau = src.next()) >= 0) nxt = task_of(ntau);
-            if (next_head || ntau >= 0) {
-                const Task k = next_head ? cur : nxt;
-                const int hs = next_head ? h + 1 : nxt.hk * p.G;
-                stage(k, hs, !next_head, false);
-                const Gv gv = gates_load(k, hs);
-                if (next_head) ghead = gv;
-                else gnext = gv;
-            }
-        }
         // 11. the record, every warp (lanes 32 (warp % 4) .., the 16-column chunks warp / 4 + 4 j, j = 0..3: two of
         //     [W; P W] and two of [U; P U], so that every warp has the same share of the costlier first kind),
         //     in fp16: W rows -> rows 0..63 of the [W; Qe] operand; P W rows -> Qe = e^gamma q_hat - P W, rows
@@ -754,9 +781,9 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     }
     if (!ok) break;
     src.done(blk, hk);   // the task's record is complete
-    if (ntau < 0) break;
+    if ((ntau = src.next()) < 0) break;
     tau = ntau;
-    cur = nxt;
+    cur = *reinterpret_cast<const Task *>(sm + OFF_NEXT);
     blk = cur.blk; hk = cur.hk; n = cur.n;
     gates_store(gnext);
     }   // tasks
@@ -764,8 +791,8 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     if (!ok) {   // a bounded wait ran out: record it and wait (bounded) for what is still in flight
         if (t == 0) {
             atomicOr(p.err, 1u);
-            if (in_pending && p.debug_skip_first_copy != 2) mbar_wait_bounded(&bar[0], in_phase, p.wait_limit);
-            if (mma_pending) mbar_wait_bounded(&bar[1], mma_phase, p.wait_limit);
+            if (in_pending && p.debug_skip_first_copy != 2) mbar_wait_bounded(&bar[0], in_phase, wait_limit);
+            if (mma_pending) mbar_wait_bounded(&bar[1], mma_phase, wait_limit);
         }
         tc_fence_before();
         __syncthreads();
