@@ -71,6 +71,10 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     prefill_fused_kernel(const __grid_constant__ LaunchCommon p, int64_t ch, const FusedArgs f) {
     extern __shared__ __align__(1024) unsigned char sm[];
     grid_dep_launch();   // every CTA of this launch has started: the next kernel may take SMs as ours leave
+    if ((int)blockIdx.x >= f.n_chain && threadIdx.x == 32) {   // a prologue CTA's first task's inputs into L2
+        const int pc = (int)blockIdx.x - f.n_chain;
+        if (pc < (p.nblk - p.blk_lo) * p.Hk) prefetch_task_inputs(p, p.blk_lo + pc / p.Hk, pc % p.Hk);
+    }
     grid_dep_wait();     // the states, conv states and workspace of earlier work
     if ((int)blockIdx.x < f.n_chain) {
         FlagReady ready{f.flags, f.epoch, p.Hk, p.wait_limit};

@@ -12,17 +12,8 @@ __global__ void __launch_bounds__(kUmmaPrepThreads, 1)
     extern __shared__ __align__(1024) unsigned char sm[];
     UmmaCtl *ctl = reinterpret_cast<UmmaCtl *>(sm + up::OFF_BAR);
     const int nbt = p.nblk - p.blk_lo;   // blocks of this launch's tasks
-    if (threadIdx.x == 32 && (int)blockIdx.x < nbt * p.Hk) {
-        // The first task's input tiles and gates into L2 while this CTA waits for earlier work. A prefetch only
-        // places lines in L2, the point of coherence, so a write that lands later still wins.
-        const int blk = p.blk_lo + (int)blockIdx.x % nbt, hk = (int)blockIdx.x / nbt;
-        const SessRef s = p.s[find_session(p, blk)];
-        const int pos0 = (blk - s.blk0) * kBlock, row0 = (int)(s.row0 + pos0);
-        tma_prefetch_2d(&p.tm_q, hk * up::D, row0);
-        tma_prefetch_2d(&p.tm_k, hk * up::D, row0);
-        for (int gi = 0; gi < p.G; ++gi) tma_prefetch_2d(&p.tm_v, (hk * p.G + gi) * up::D, row0);
-        prefetch_gates(p, row0, min(kBlock, s.n - pos0));
-    }
+    if (threadIdx.x == 32 && (int)blockIdx.x < nbt * p.Hk)   // the first task's inputs, while waiting below
+        prefetch_task_inputs(p, p.blk_lo + (int)blockIdx.x % nbt, (int)blockIdx.x / nbt);
     if ((threadIdx.x >> 5) == 0) {
         tmem_alloc(&ctl->tslot, 512);
         tmem_relinquish();

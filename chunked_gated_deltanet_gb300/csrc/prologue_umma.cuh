@@ -173,6 +173,17 @@ __device__ __forceinline__ void prefetch_gates(const LaunchCommon &p, int64_t ro
     }
 }
 
+// Task (blk, hk)'s input tiles and gates into L2, for a CTA's first task while it waits for earlier work.
+// A prefetch only places lines in L2, the point of coherence, so a write that lands later still wins.
+__device__ __forceinline__ void prefetch_task_inputs(const LaunchCommon &p, int blk, int hk) {
+    const SessRef s = p.s[find_session(p, blk)];
+    const int pos0 = (blk - s.blk0) * kBlock, row0 = (int)(s.row0 + pos0);
+    tma_prefetch_2d(&p.tm_q, hk * up::D, row0);
+    tma_prefetch_2d(&p.tm_k, hk * up::D, row0);
+    for (int gi = 0; gi < p.G; ++gi) tma_prefetch_2d(&p.tm_v, (hk * p.G + gi) * up::D, row0);
+    prefetch_gates(p, row0, min(kBlock, s.n - pos0));
+}
+
 // named barrier `id` over n threads (whole warps): bar_sync waits, bar_arrive only signals (its earlier
 // shared-memory writes are visible to the threads that wait on the same barrier)
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
