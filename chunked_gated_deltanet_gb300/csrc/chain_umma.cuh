@@ -307,10 +307,31 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
             // 32-byte stores where the output allows them (every 8-column group of a row starts on a 32-byte
             // boundary when the output does)
             const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
-#pragma unroll 1
+            // with up to 32 columns per thread every TMEM load of the step goes out before the one wait
+            constexpr bool kAllAtOnce = NC <= 32;
+            float zall[kAllAtOnce ? NC : 1];
+            if constexpr (kAllAtOnce) {
+                uint32_t ra[NC / 16][16], rb[NC / 16][16];
+#pragma unroll
+                for (int j16 = 0; j16 < NC / 16; ++j16) {
+                    tmem_ld16_nowait(tl + cl + 16 * j16, ra[j16]);
+                    tmem_ld16_nowait(tl + N + cl + 16 * j16, rb[j16]);
+                }
+#pragma unroll
+                for (int j16 = 0; j16 < NC / 16; ++j16) {
+                    tmem_wait_ld(ra[j16]);
+                    tmem_wait_ld(rb[j16]);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) zall[16 * j16 + c] = __uint_as_float(ra[j16][c]) + __uint_as_float(rb[j16][c]);
+                }
+            }
+#pragma unroll
             for (int j16 = 0; j16 < NC / 16; ++j16) {
                 float z[16];
-                {
+                if constexpr (kAllAtOnce) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) z[c] = zall[16 * j16 + c];
+                } else {
                     uint32_t ra[16], rb[16];
                     tmem_ld16_nowait(tl + cl + 16 * j16, ra);
                     tmem_ld16_nowait(tl + N + cl + 16 * j16, rb);
