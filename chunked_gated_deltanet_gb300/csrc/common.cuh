@@ -30,8 +30,9 @@ struct LaunchCommon {
     const float *g, *beta;      // [rows][Hv]
     const void *conv_w;         // [ch][4]
     void *out;                  // [rows][Hv][D]
-    float *ws_qk;               // [nblk][Hk][2][64][D]   q_hat, k_hat
-    float *ws_wu;               // [nblk][Hv][wu_floats]  W, U, P, gamma
+    float *ws_qk;               // fp32 path: [nblk][Hk][2][64][D] q_hat, k_hat
+    float *ws_wu;               // per (block, v-head) record: fp32 path [wu_floats] W, U, P, gamma; bf16 paths
+                                // the layouts of their state kernels (rec16::kBytes for d = 128)
     int Hk, Hv, G;
     int act, out_bf16;
     float q_scale, eps;

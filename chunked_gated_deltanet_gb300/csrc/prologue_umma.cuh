@@ -216,8 +216,8 @@ __device__ __forceinline__ void join8(uint4 hi, uint4 lo, float *v) {
 
 // Runs the tasks that `src` hands out, in order, on the operand plan at `sm` with control words `ctl` and
 // 512 TMEM columns at `tmem` (allocated by the caller); every thread of the CTA (512) calls it. A task is
-// one (64-token block, q/k head) with each of the head's G v-heads; the next task's inputs are staged
-// during the current task's record epilogue. Returns false if a bounded wait ran out (the error word is
+// one (64-token block, q/k head) with each of the head's G v-heads; the next head's or task's inputs are
+// staged while the current head's inverse runs. Returns false if a bounded wait ran out (the error word is
 // set, nothing is left in flight). The mbarriers are initialised on entry and invalidated on return, so
 // the plan's memory may serve other uses between calls.
 template <bool kAct, class Src>
@@ -549,7 +549,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
     // 4. each v-head of the group
     for (int gi = 0; ok && gi < G; ++gi) {
         const int h = hk * G + gi;
-        if (gi > 0) {   // this head's v tile was staged during the previous head's record epilogue
+        if (gi > 0) {   // this head's v tile was staged while the previous head's inverse ran
             gates_store(ghead);
             if (!(ok = wait_in())) break;
         }
