@@ -44,7 +44,7 @@ PRECISION = {"inputs": "bf16", "conv_norm_gates": "fp32",
              "prologue_products": "tcgen05 kind::f16, fp32 accumulate: [q; k] k^T on bf16 hi/lo operand pairs "
                                   "(hi*hi + hi*lo + lo*hi); P T and [T; P T] [beta e^gamma k | beta v] on single fp16 "
                                   "operands",
-             "triangular_inverse": "fp32 substitution + split-tf32 products",
+             "triangular_inverse": "fp32 substitution + tf32 products",
              "record": "fp16 (W, Qe, K_tilde, U, O_intra) and fp32 e^gamma",
              "state_pass_products": "tcgen05 kind::f16: fp16 operands (record, state copy, U'), fp32 accumulate",
              "state": "fp32", "outputs": "fp32"}

@@ -28,7 +28,7 @@
 // row-ordered operands (q_hat, k_hat, P, T, P T) K-major, the token-by-channel
 // B operands MN-major, so that every producer writes whole 16-byte
 // core-matrix rows. The triangular inverse stays in fp32: substitution on the
-// CUDA cores for its 16 x 16 diagonal blocks, split-tf32 mma.sync for the
+// CUDA cores for its 16 x 16 diagonal blocks, tf32 mma.sync for the
 // blocked products. The input tiles arrive as 2-D tensor copies (one per tile)
 // plus three single-row halo copies, on an mbarrier: a task's tiles are
 // copied in during the inverse of the task before it (their region is their
@@ -127,38 +127,25 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 // the two bf16 values of a 32-bit word as an fp32 pair (low half first)
 __device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t u) { return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u)); }
 
-// x = hi + lo exactly, hi the tf32 truncation of x (low 13 bits cleared), lo the rest in fp32. The MMA
-// reads lo as tf32 by dropping its low 13 bits, so a split product misses at most about 2^-20 |x| of each
-// operand: far below the bf16 hi/lo split (about 2^-16) that the inverse's result goes through next.
-__device__ __forceinline__ void split_tf32_trunc(float x, uint32_t &hi, uint32_t &lo) {
-    hi = __float_as_uint(x) & 0xFFFFE000u;
-    lo = __float_as_uint(x - __uint_as_float(hi));
-}
-
 // c = X Y for a 16 x K block of X (row-major, pitch lx) and a K x 8 block of Y (row-major, pitch ly), K a
-// multiple of 8, m16n8k8 tf32 MMAs with split operands (hi*hi + hi*lo + lo*hi: close to fp32 products); one
-// warp. The three partial products accumulate apart, so the dependent chain is K / 8 MMAs long, and the two
-// small ones are added together before they join the large one. The k loop stays rolled: its chain is
+// multiple of 8: m16n8k8 tf32 MMAs, operands rounded to tf32 (to nearest), fp32 accumulation; one warp. The
+// inverse's result is rounded to fp16 before every use, so products at tf32 precision leave the layer's error
+// where it is (a CPU emulation of the blocked inverse on the workloads' inputs: 4.22e-4 / 4.26e-4 against
+// 4.21e-4 / 4.32e-4 for fp32 products, outputs / state). The k loop stays rolled: its chain is
 // latency-bound either way, and the compact code keeps the caller's loop within the instruction caches.
-__device__ __forceinline__ void mma3_tf32_16x8(float (&c)[4], const float *X, int lx, const float *Y, int ly, int K,
-                                               int lane) {
+__device__ __forceinline__ void mma_tf32_16x8(float (&c)[4], const float *X, int lx, const float *Y, int ly, int K,
+                                              int lane) {
     const int g = lane >> 2, t = lane & 3;
-    float hh[4] = {0.f, 0.f, 0.f, 0.f}, hl[4] = {0.f, 0.f, 0.f, 0.f}, lh[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int k0 = 0; k0 < K; k0 += 8) {
-        uint32_t ah[4], al[4], bh[2], bl[2];
-        split_tf32_trunc(X[g * lx + k0 + t], ah[0], al[0]);
-        split_tf32_trunc(X[(g + 8) * lx + k0 + t], ah[1], al[1]);
-        split_tf32_trunc(X[g * lx + k0 + t + 4], ah[2], al[2]);
-        split_tf32_trunc(X[(g + 8) * lx + k0 + t + 4], ah[3], al[3]);
-        split_tf32_trunc(Y[(k0 + t) * ly + g], bh[0], bl[0]);
-        split_tf32_trunc(Y[(k0 + t + 4) * ly + g], bh[1], bl[1]);
-        mma_tf32(lh, al, bh);
-        mma_tf32(hl, ah, bl);
-        mma_tf32(hh, ah, bh);
+        const uint32_t a[4] = {tf32_bits(X[g * lx + k0 + t]), tf32_bits(X[(g + 8) * lx + k0 + t]),
+                               tf32_bits(X[g * lx + k0 + t + 4]), tf32_bits(X[(g + 8) * lx + k0 + t + 4])};
+        const uint32_t b[2] = {tf32_bits(Y[(k0 + t) * ly + g]), tf32_bits(Y[(k0 + t + 4) * ly + g])};
+        mma_tf32(acc, a, b);
     }
 #pragma unroll
-    for (int f = 0; f < 4; ++f) c[f] = hh[f] + (hl[f] + lh[f]);
+    for (int f = 0; f < 4; ++f) c[f] = acc[f];
 }
 // The gates (g and beta, [rows][Hv] fp32) of rows [row0, row0 + n) into L2: the whole 16-byte granules
 // inside those rows only, so that the prefetch stays within the rows the task reads.
@@ -631,7 +618,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
         if (stage_next) in_pending = 1;
 
         // 7. T = (I + A)^{-1} (unit lower triangular) in fp32, two levels of 2x2 blocking, products as
-        //    split-tf32 MMAs, one 16 x 8 tile per warp:
+        //    tf32 MMAs, one 16 x 8 tile per warp:
         //    (a) diagonal 16x16 blocks D_b by substitution, one column per thread (warp 0: D_0, D_1; warp 1:
         //        D_2, D_3); warps 8-15 zero the blocks above the diagonal, then issue the copies above;
         //    (b) warps 0-3 (block pair (b + 1, b), column tile nt): T_10 = -D_1 (A_10 D_0), T_32 = -D_3 (A_32 D_2);
@@ -680,10 +667,10 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             const int b = 2 * (warp >> 1), nt = warp & 1;
             float *M = Mt + (warp >> 1) * 16 * LM;
             float cc[4];
-            mma3_tf32_16x8(cc, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, 16, lane);
+            mma_tf32_16x8(cc, Af + 16 * (b + 1) * LT + 16 * b, LT, Tf + 16 * b * LT + 16 * b + 8 * nt, LT, 16, lane);
             store_c16x8(M + 8 * nt, LM, cc, 1.f, lane);
             __syncwarp();
-            mma3_tf32_16x8(cc, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, M + 8 * nt, LM, 16, lane);
+            mma_tf32_16x8(cc, Tf + 16 * (b + 1) * LT + 16 * (b + 1), LT, M + 8 * nt, LM, 16, lane);
             store_c16x8(Tf + 16 * (b + 1) * LT + 16 * b + 8 * nt, LT, cc, -1.f, lane);
         }
         if (warp < 8) {   // (c)
@@ -692,7 +679,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             float cc[4];
             // T[0:16, 16:32] = 0: column tiles 2 and 3 of T[0:32, 0:32] need only its rows 16..31
             const int k0 = nt < 2 ? 0 : 16;
-            mma3_tf32_16x8(cc, Af + (32 + 16 * mt) * LT + k0, LT, Tf + k0 * LT + 8 * nt, LT, 32 - k0, lane);
+            mma_tf32_16x8(cc, Af + (32 + 16 * mt) * LT + k0, LT, Tf + k0 * LT + 8 * nt, LT, 32 - k0, lane);
             store_c16x8(Xs + 16 * mt * LX + 8 * nt, LX, cc, 1.f, lane);
             // T[32:48, 48:64] = 0: row tile 0 needs only X rows 0..15 (its own tile), row tile 1 all 32
             if (mt == 0) {
@@ -701,7 +688,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             } else {
                 bar_sync(3 + nt, 64);
             }
-            mma3_tf32_16x8(cc, Tf + (32 + 16 * mt) * LT + 32, LT, Xs + 8 * nt, LX, 16 + 16 * mt, lane);
+            mma_tf32_16x8(cc, Tf + (32 + 16 * mt) * LT + 32, LT, Xs + 8 * nt, LX, 16 + 16 * mt, lane);
             store_c16x8(Tf + (32 + 16 * mt) * LT + 8 * nt, LT, cc, -1.f, lane);
         }
         __syncthreads();
