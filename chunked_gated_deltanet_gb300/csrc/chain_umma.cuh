@@ -322,7 +322,10 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
                     tmem_wait_ld(ra[j16]);
                     tmem_wait_ld(rb[j16]);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) zall[16 * j16 + c] = __uint_as_float(ra[j16][c]) + __uint_as_float(rb[j16][c]);
+                    for (int c = 0; c < 16; c += 2)   // packed pairs: each lane rounds as the scalar add does
+                        f2_unpack(f2_add(f2_pack(__uint_as_float(ra[j16][c]), __uint_as_float(ra[j16][c + 1])),
+                                         f2_pack(__uint_as_float(rb[j16][c]), __uint_as_float(rb[j16][c + 1]))),
+                                  zall[16 * j16 + c], zall[16 * j16 + c + 1]);
                 }
             }
 #pragma unroll
@@ -347,12 +350,15 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
                     h8_to_f(*reinterpret_cast<const uint4 *>(uo + ((cl >> 3) + j) * 1024), v);
                     if (q < 2) {   // U' = U - Z[0:64] for token row `row`, as fp16 into the MN-major B operand of dS
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] -= z[8 * hf + e];
+                        for (int e = 0; e < 8; e += 2)   // v - z as one rounding: fma(z, -1, v)
+                            f2_unpack(f2_fma(f2_pack(z[8 * hf + e], z[8 * hf + e + 1]), f2_pack(-1.f, -1.f), f2_pack(v[e], v[e + 1])),
+                                      v[e], v[e + 1]);
                         *reinterpret_cast<uint4 *>(UB + ((cl >> 3) + j) * P::kSBO_U + (row >> 3) * 128 + (row & 7) * 16) =
                             f8_to_h8(v);
                     } else if (out_row) {   // O = Z[64:128] + O_intra for token row i
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] += z[8 * hf + e];
+                        for (int e = 0; e < 8; e += 2)
+                            f2_unpack(f2_add(f2_pack(v[e], v[e + 1]), f2_pack(z[8 * hf + e], z[8 * hf + e + 1])), v[e], v[e + 1]);
                         if (p.out_bf16) {
                             const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), bb = __floats2bfloat162_rn(v[2], v[3]),
                                                  c = __floats2bfloat162_rn(v[4], v[5]), d = __floats2bfloat162_rn(v[6], v[7]);
@@ -388,8 +394,9 @@ __device__ __forceinline__ void chain_run(const LaunchCommon &p, int64_t ch, uns
                 float d[NC];
                 tmem_ld_cols<NC>(tl + 2 * N + cl, d);
                 const float e = *reinterpret_cast<const float *>(stg + P::kEgOff);
+                const uint64_t e2 = f2_pack(e, e);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) st[c] = fmaf(e, st[c], d[c]);
+                for (int c = 0; c < NC; c += 2) f2_unpack(f2_fma(e2, f2_pack(st[c], st[c + 1]), f2_pack(d[c], d[c + 1])), st[c], st[c + 1]);
                 write_S();
             }
             fence_proxy_async();

@@ -106,24 +106,6 @@ struct StridedTasks {
     __device__ __forceinline__ void done(int, int) {}
 };
 
-// Packed fp32 pairs (sm_100 and later): each lane rounds as the scalar instruction does, so a pair of
-// scalar mul / fma chains and its packed form give the same bits.
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t r, float &a, float &b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r)); }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
 // the two bf16 values of a 32-bit word as an fp32 pair (low half first)
 __device__ __forceinline__ uint64_t f2_from_bf16x2(uint32_t u) { return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u)); }
 
