@@ -177,10 +177,8 @@ __device__ __forceinline__ void split8(const float *v, uint4 &hi, uint4 &lo) {
 __device__ __forceinline__ void join8(uint4 hi, uint4 lo, float *v) {
     const uint32_t h[4] = {hi.x, hi.y, hi.z, hi.w}, l[4] = {lo.x, lo.y, lo.z, lo.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        v[2 * q] = __uint_as_float(h[q] << 16) + __uint_as_float(l[q] << 16);
-        v[2 * q + 1] = __uint_as_float(h[q] & 0xFFFF0000u) + __uint_as_float(l[q] & 0xFFFF0000u);
-    }
+    for (int q = 0; q < 4; ++q)   // packed pairs (the same bits as two scalar adds)
+        f2_unpack(f2_add(f2_from_bf16x2(h[q]), f2_from_bf16x2(l[q])), v[2 * q], v[2 * q + 1]);
 }
 
 // Runs the tasks that `src` hands out, in order, on the operand plan at `sm` with control words `ctl` and
@@ -432,7 +430,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
             join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), v);
             const float sc = bet[j] * egv[j];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) v[c] *= sc;
+            for (int c = 0; c < 8; c += 2) f2_unpack(f2_mul(f2_pack(v[c], v[c + 1]), f2_pack(sc, sc)), v[c], v[c + 1]);
             *reinterpret_cast<uint4 *>(Bh + mnmajor_bf16_offset(8 * cg, j, B_LBO, B_SBO)) = f8_to_h8(v);
         }
     };
@@ -538,7 +536,7 @@ __device__ __forceinline__ bool prologue_run(const LaunchCommon &p, int64_t ch, 
                 join8(*reinterpret_cast<const uint4 *>(AQh + o), *reinterpret_cast<const uint4 *>(AQl + o), v);
                 const float dec = __expf(gl - gam[j]);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) v[c] *= dec;
+                for (int c = 0; c < 8; c += 2) f2_unpack(f2_mul(f2_pack(v[c], v[c + 1]), f2_pack(dec, dec)), v[c], v[c + 1]);
                 *reinterpret_cast<uint4 *>(rec + rec16::kt(8 * dg, j)) = f8_to_h8(v);
             }
             if (part == 0 && t == 32) *reinterpret_cast<float *>(rec + rec16::kEg) = expf(gl);
